@@ -1,0 +1,195 @@
+/*
+ * dsa_mla.h: C ABI of libdsa_mla, the GB300 (sm_103a) selected-index NoPE MLA paged
+ * decode.
+ *
+ * Source pages (cited by title and item):
+ *   [attend.rs]   spark_model/layers/glm5next_dsa/attend.rs
+ *   [decode_k.rs] metrale_model_arch/glm5next_dsa/layer/decode_k.rs
+ *
+ * What is computed (attend.rs, module doc and decode_attention). For every decode row r
+ * (sequence seq = r / rows_per_seq) and query head h:
+ *   S_r       = distinct ids j of sel_indices[r, :] with 0 <= j < seq_len(r)
+ *               (-1 and any other id outside [0, seq_len(r)) is a hole; duplicates
+ *               count once: set membership, not a weighting)
+ *   K_j = V_j = the 512-byte E4M3 latent row of token j, at byte
+ *               block_tables[seq*max_blocks_per_seq + j/block_size]*cache_stride_bytes
+ *               + (j % block_size)*512 of k_cache (resp. v_cache)
+ *   out[r,h,:] = sum_{j in S_r} softmax_j(sm_scale * q[r,h,:].(k_scale*K_j)) (v_scale*V_j)
+ *               and 0 when S_r is empty.
+ * kv_lora_rank is fixed at 512 and there is one latent KV head with no rope section
+ * (attend.rs, "NoPE, and why no common/ kernel would do"; DsaDecodePaging::validate).
+ *
+ * Conventions for every entry point:
+ *  - Device pointers are caller-owned CUDA device memory on the current device; the
+ *    library never frees or keeps them. "stream" is a cudaStream_t passed as void*.
+ *  - Calls enqueue work on the stream and return without synchronising (attend.rs,
+ *    decode_attention: "Enqueued on stream, not synchronised"), except where stated.
+ *  - Arguments are checked on the host before anything is enqueued; an invalid call
+ *    returns its status and writes nothing.
+ *  - A missing or unloadable kernel is a hard error (DSA_ERR_NO_KERNEL), never a
+ *    fallback to another path (attend.rs, Glm5NextDsaDecodeKernel::resolve).
+ *  - Problems only visible on the device (a block-table entry that is negative or past
+ *    max_blocks_per_seq, a pipeline wait that ran out of time) do not fault: the kernel
+ *    skips the access and records the first such status in the workspace's status
+ *    word, read back with dsa_read_device_status / dsa_last_device_status. The output
+ *    of a call that recorded a device status is undefined.
+ */
+#ifndef DSA_MLA_H
+#define DSA_MLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum dsa_status {
+    DSA_OK = 0,
+    DSA_ERR_INVALID_ARGUMENT = 1, /* bad pointer, size, alignment or stride */
+    DSA_ERR_UNSUPPORTED = 2,      /* device is not sm_103, or a size beyond the limits below */
+    DSA_ERR_WORKSPACE = 3,        /* workspace too small, or growth needed during graph capture */
+    DSA_ERR_CUDA = 4,             /* a CUDA runtime call or launch failed */
+    DSA_ERR_NO_KERNEL = 5,        /* the sm_103a kernel image is missing for this device */
+    DSA_ERR_DEVICE_BOUNDS = 6,    /* device-side: a page lookup fell outside the block table */
+    DSA_ERR_TIMEOUT = 7           /* device-side: a pipeline wait exceeded its time limit */
+} dsa_status;
+
+/* Limits. sel_width may not exceed DSA_MAX_SEL_WIDTH. */
+#define DSA_LATENT_DIM 512
+#define DSA_MAX_SEL_WIDTH 8192
+
+/* Version of this ABI (incremented on any incompatible change). */
+int32_t dsa_abi_version(void);
+
+/* Static description of a status code. Never NULL. */
+const char* dsa_status_string(int32_t status);
+
+/*
+ * dsa_mla_decode: the selected-index decode (attend.rs, decode_attention).
+ *
+ *  q                  bf16 [R, num_q_heads, 512], R = num_seqs * rows_per_seq, rows ordered
+ *                     seq*rows_per_seq + i; absorbed queries in latent space (attend.rs,
+ *                     DsaDecodeInputs::q). 16-byte aligned.
+ *  k_cache, v_cache   E4M3 paged latent cache; page p starts at byte p*cache_stride_bytes.
+ *                     K and V are normally the same buffer (attend.rs, DsaDecodeInputs:
+ *                     "K and V are the same buffer"); distinct buffers are read separately.
+ *                     16-byte aligned, non-NULL.
+ *  block_tables       int32 page ids; the table of sequence s starts at
+ *                     block_tables + s*max_blocks_per_seq (max_blocks_per_seq = 0: every
+ *                     sequence reads the one table at block_tables, decode_k.rs decode_k).
+ *  max_blocks_per_seq block-table row stride in entries (>= 0). When > 0, a lookup past
+ *                     it is a device-side DSA_ERR_DEVICE_BOUNDS.
+ *  seq_lens           int32 [R]: row r only sees token positions < seq_lens[r].
+ *  sel_indices        int32 [R, sel_width] selected token ids, -1 = hole.
+ *  sel_width          1..DSA_MAX_SEL_WIDTH.
+ *  num_seqs, rows_per_seq, num_q_heads  >= 1.
+ *  block_size         tokens per page, >= 1.
+ *  cache_stride_bytes bytes per page, >= block_size*512 and a multiple of 16
+ *                     (block_size*512 for a dense pool: decode_k.rs, cache_stride_bytes).
+ *  k_scale, v_scale   cache dequantisation scales (attend.rs, DsaDecodeInputs).
+ *  sm_scale           score scale; the pages pass kv_lora_rank^-0.5 (attend.rs,
+ *                     decode_attention, "the score scale is over the latent width").
+ *  out                bf16 [R, num_q_heads, 512], latent space. 16-byte aligned.
+ *
+ * Uses a library-owned workspace per device, grown on demand with cudaMalloc; growing
+ * it while the stream is being captured into a graph returns DSA_ERR_WORKSPACE (use
+ * dsa_mla_decode_ws with caller memory for capture).
+ */
+int32_t dsa_mla_decode(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                       const int32_t* seq_lens, const int32_t* sel_indices, int32_t sel_width,
+                       int32_t num_seqs, int32_t rows_per_seq, int32_t num_q_heads,
+                       int32_t block_size, int64_t cache_stride_bytes, float k_scale,
+                       float v_scale, float sm_scale, void* out, void* stream);
+
+/*
+ * dsa_mla_decode_k: k consecutive verify rows per sequence (decode_k.rs, decode_k and
+ * attend_rows). Arguments as dsa_mla_decode with rows_per_seq = k, except:
+ *  seq_lens  int32 [num_seqs]: the sequence length seq_len before the k new tokens.
+ *            Row i (0 <= i < k) of sequence s sits at position seq_len + i and sees
+ *            positions < seq_lens[s] + i + 1 (decode_k.rs: "sl[row] = pos + 1").
+ * All k rows of a sequence share its block table.
+ */
+int32_t dsa_mla_decode_k(const void* q, const void* k_cache, const void* v_cache,
+                         const int32_t* block_tables, int32_t max_blocks_per_seq,
+                         const int32_t* seq_lens, const int32_t* sel_indices, int32_t sel_width,
+                         int32_t num_seqs, int32_t k, int32_t num_q_heads, int32_t block_size,
+                         int64_t cache_stride_bytes, float k_scale, float v_scale,
+                         float sm_scale, void* out, void* stream);
+
+/*
+ * Bytes of caller workspace dsa_mla_decode_ws needs for this shape. num_ctas is the
+ * decode grid size to plan for (0 = the default for the current device, which needs a
+ * CUDA device; returns 0 if none is available).
+ */
+size_t dsa_mla_decode_workspace_bytes(int32_t num_seqs, int32_t rows_per_seq,
+                                      int32_t num_q_heads, int32_t sel_width, int32_t num_ctas);
+
+/*
+ * dsa_mla_decode_ws: dsa_mla_decode / dsa_mla_decode_k with caller-owned workspace
+ * (device memory, 256-byte aligned, >= dsa_mla_decode_workspace_bytes for the same
+ * shape and num_ctas). Never allocates, so it can be captured into a CUDA graph.
+ *  verify_rows   0: seq_lens is per row (dsa_mla_decode); 1: seq_lens is per sequence
+ *                and rows follow the verify rule (dsa_mla_decode_k).
+ *  num_ctas      decode grid size, 0 = default (the SM count, fewer for small problems).
+ *  ev_begin, ev_end  optional cudaEvent_t (as void*, NULL = none) recorded on the stream
+ *                immediately before and after the main decode kernel.
+ * The first 256 bytes of the workspace hold the device status word of the latest call.
+ */
+int32_t dsa_mla_decode_ws(const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_tables, int32_t max_blocks_per_seq,
+                          const int32_t* seq_lens, const int32_t* sel_indices, int32_t sel_width,
+                          int32_t num_seqs, int32_t rows_per_seq, int32_t num_q_heads,
+                          int32_t block_size, int64_t cache_stride_bytes, float k_scale,
+                          float v_scale, float sm_scale, void* out, int32_t verify_rows,
+                          void* workspace, size_t workspace_bytes, int32_t num_ctas,
+                          void* ev_begin, void* ev_end, void* stream);
+
+/*
+ * dsa_mla_decode_host: the same decode with the per-step inputs and the output in HOST
+ * memory (pinned for asynchronous copies). The caches stay device-resident. The call
+ * copies q, block_tables (table_rows * max(max_blocks_per_seq,1) entries), seq_lens and
+ * sel_indices into device staging inside `workspace`, runs the decode and copies out
+ * back, all on `stream`; the output is valid after the stream synchronises.
+ *  table_rows   rows of block_tables to copy (num_seqs, or 1 for a shared table).
+ *  workspace    >= dsa_mla_decode_host_workspace_bytes(...).
+ */
+size_t dsa_mla_decode_host_workspace_bytes(int32_t num_seqs, int32_t rows_per_seq,
+                                           int32_t num_q_heads, int32_t sel_width,
+                                           int32_t table_rows, int32_t max_blocks_per_seq,
+                                           int32_t verify_rows, int32_t num_ctas);
+int32_t dsa_mla_decode_host(const void* q_host, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables_host, int32_t table_rows,
+                            int32_t max_blocks_per_seq, const int32_t* seq_lens_host,
+                            const int32_t* sel_indices_host, int32_t sel_width, int32_t num_seqs,
+                            int32_t rows_per_seq, int32_t num_q_heads, int32_t block_size,
+                            int64_t cache_stride_bytes, float k_scale, float v_scale,
+                            float sm_scale, void* out_host, int32_t verify_rows,
+                            void* workspace, size_t workspace_bytes, int32_t num_ctas,
+                            void* stream);
+
+/*
+ * dsa_resolve_indices: the index resolution step on its own (attend.rs module doc: -1
+ * holes, set membership with duplicates collapsed). For each row: the distinct ids
+ * 0 <= id < seq_lens[r] in ascending order, then -1 padding to sel_width.
+ *  ids_out     int32 [rows, sel_width]; counts_out int32 [rows].
+ */
+int32_t dsa_resolve_indices(const int32_t* sel_indices, const int32_t* seq_lens,
+                            int32_t sel_width, int32_t rows, int32_t* ids_out,
+                            int32_t* counts_out, void* stream);
+
+/*
+ * Device status of the latest call on a caller workspace (dsa_mla_decode_ws /
+ * dsa_mla_decode_host) or on the library workspace of the current device
+ * (dsa_last_device_status). Synchronises the stream, writes the status to *status_out
+ * and returns DSA_OK, or returns DSA_ERR_CUDA.
+ */
+int32_t dsa_read_device_status(const void* workspace, int32_t* status_out, void* stream);
+int32_t dsa_last_device_status(int32_t* status_out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_MLA_H */

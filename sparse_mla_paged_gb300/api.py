@@ -1,0 +1,184 @@
+"""Python binding of the C ABI (include/dsa_mla.h): argument marshalling only.
+
+Every step of the decode runs in the library's sm_103a kernels; these functions pass
+torch tensors' device pointers, sizes and the current CUDA stream through ctypes and
+raise DsaError on a non-OK status.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import _lib
+from ._lib import DsaError, check  # noqa: F401
+
+LATENT = 512
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _need(t: torch.Tensor, dtype, name: str):
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor of {dtype}")
+
+
+def abi_version() -> int:
+    return int(_lib.load().dsa_abi_version())
+
+
+def status_string(status: int) -> str:
+    return _lib.load().dsa_status_string(int(status)).decode()
+
+
+def _decode_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, sel_indices, num_seqs,
+                 rows_per_seq, num_q_heads, block_size, cache_stride_bytes, k_scale, v_scale, sm_scale, out):
+    _need(q, torch.bfloat16, "q")
+    _need(k_cache, torch.uint8, "k_cache")
+    _need(v_cache, torch.uint8, "v_cache")
+    _need(block_tables, torch.int32, "block_tables")
+    _need(seq_lens, torch.int32, "seq_lens")
+    _need(sel_indices, torch.int32, "sel_indices")
+    _need(out, torch.bfloat16, "out")
+    return [_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), int(max_blocks_per_seq), _ptr(seq_lens),
+            _ptr(sel_indices), int(sel_indices.shape[-1]), int(num_seqs), int(rows_per_seq), int(num_q_heads),
+            int(block_size), int(cache_stride_bytes), float(k_scale), float(v_scale), float(sm_scale), _ptr(out)]
+
+
+def _out_like(q, out):
+    return torch.empty_like(q) if out is None else out
+
+
+def decode(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, sel_indices, num_seqs,
+           rows_per_seq, num_q_heads, block_size, cache_stride_bytes, k_scale, v_scale, sm_scale,
+           out=None, stream=None) -> torch.Tensor:
+    """dsa_mla_decode: per-row seq_lens; returns out (bf16 [R, H, 512])."""
+    out = _out_like(q, out)
+    a = _decode_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, sel_indices, num_seqs,
+                     rows_per_seq, num_q_heads, block_size, cache_stride_bytes, k_scale, v_scale, sm_scale, out)
+    check(_lib.load().dsa_mla_decode(*a, _stream(stream)), "dsa_mla_decode")
+    return out
+
+
+def decode_k(q, k_cache, v_cache, block_tables, max_blocks_per_seq, base_lens, sel_indices, num_seqs, k,
+             num_q_heads, block_size, cache_stride_bytes, k_scale, v_scale, sm_scale, out=None,
+             stream=None) -> torch.Tensor:
+    """dsa_mla_decode_k: k verify rows per sequence; base_lens is per sequence."""
+    out = _out_like(q, out)
+    a = _decode_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq, base_lens, sel_indices, num_seqs, k,
+                     num_q_heads, block_size, cache_stride_bytes, k_scale, v_scale, sm_scale, out)
+    check(_lib.load().dsa_mla_decode_k(*a, _stream(stream)), "dsa_mla_decode_k")
+    return out
+
+
+def workspace_bytes(num_seqs, rows_per_seq, num_q_heads, sel_width, num_ctas=0) -> int:
+    return int(_lib.load().dsa_mla_decode_workspace_bytes(int(num_seqs), int(rows_per_seq), int(num_q_heads),
+                                                          int(sel_width), int(num_ctas)))
+
+
+def alloc_workspace(num_seqs, rows_per_seq, num_q_heads, sel_width, num_ctas=0, device=None) -> torch.Tensor:
+    n = workspace_bytes(num_seqs, rows_per_seq, num_q_heads, sel_width, num_ctas)
+    if n == 0:
+        raise DsaError(2, "dsa_mla_decode_workspace_bytes")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def decode_ws(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, sel_indices, num_seqs,
+              rows_per_seq, num_q_heads, block_size, cache_stride_bytes, k_scale, v_scale, sm_scale, out,
+              workspace: torch.Tensor, verify_rows=0, num_ctas=0, ev_begin=None, ev_end=None,
+              stream=None) -> torch.Tensor:
+    """dsa_mla_decode_ws: caller workspace (capturable); optional events around the decode kernel."""
+    a = _decode_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, sel_indices, num_seqs,
+                     rows_per_seq, num_q_heads, block_size, cache_stride_bytes, k_scale, v_scale, sm_scale, out)
+    _need(workspace, torch.uint8, "workspace")
+    e0 = None if ev_begin is None else ev_begin.cuda_event
+    e1 = None if ev_end is None else ev_end.cuda_event
+    check(_lib.load().dsa_mla_decode_ws(*a, int(verify_rows), _ptr(workspace), workspace.numel(), int(num_ctas),
+                                        e0, e1, _stream(stream)), "dsa_mla_decode_ws")
+    return out
+
+
+def host_workspace_bytes(num_seqs, rows_per_seq, num_q_heads, sel_width, table_rows, max_blocks_per_seq,
+                         verify_rows=0, num_ctas=0) -> int:
+    return int(_lib.load().dsa_mla_decode_host_workspace_bytes(
+        int(num_seqs), int(rows_per_seq), int(num_q_heads), int(sel_width), int(table_rows),
+        int(max_blocks_per_seq), int(verify_rows), int(num_ctas)))
+
+
+def decode_host(q_host, k_cache, v_cache, block_tables_host, max_blocks_per_seq, seq_lens_host, sel_host,
+                num_seqs, rows_per_seq, num_q_heads, block_size, cache_stride_bytes, k_scale, v_scale, sm_scale,
+                out_host, workspace, verify_rows=0, num_ctas=0, stream=None) -> torch.Tensor:
+    """dsa_mla_decode_host: per-step inputs and output in (pinned) host memory."""
+    for t, n in ((q_host, "q_host"), (block_tables_host, "block_tables_host"), (seq_lens_host, "seq_lens_host"),
+                 (sel_host, "sel_host"), (out_host, "out_host")):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous host tensor")
+    _need(k_cache, torch.uint8, "k_cache")
+    _need(v_cache, torch.uint8, "v_cache")
+    check(_lib.load().dsa_mla_decode_host(
+        _ptr(q_host), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables_host), int(block_tables_host.shape[0]),
+        int(max_blocks_per_seq), _ptr(seq_lens_host), _ptr(sel_host), int(sel_host.shape[-1]), int(num_seqs),
+        int(rows_per_seq), int(num_q_heads), int(block_size), int(cache_stride_bytes), float(k_scale),
+        float(v_scale), float(sm_scale), _ptr(out_host), int(verify_rows), _ptr(workspace), workspace.numel(),
+        int(num_ctas), _stream(stream)), "dsa_mla_decode_host")
+    return out_host
+
+
+def resolve_indices(sel_indices: torch.Tensor, seq_lens: torch.Tensor, stream=None):
+    """dsa_resolve_indices -> (ids int32 [rows, W], counts int32 [rows])."""
+    _need(sel_indices, torch.int32, "sel_indices")
+    _need(seq_lens, torch.int32, "seq_lens")
+    rows, width = sel_indices.shape
+    ids = torch.empty((rows, width), dtype=torch.int32, device=sel_indices.device)
+    counts = torch.empty(rows, dtype=torch.int32, device=sel_indices.device)
+    check(_lib.load().dsa_resolve_indices(_ptr(sel_indices), _ptr(seq_lens), int(width), int(rows), _ptr(ids),
+                                          _ptr(counts), _stream(stream)), "dsa_resolve_indices")
+    return ids, counts
+
+
+def read_device_status(workspace: torch.Tensor, stream=None) -> int:
+    v = _lib.ctypes.c_int32(0)
+    check(_lib.load().dsa_read_device_status(_ptr(workspace), _lib.ctypes.byref(v), _stream(stream)),
+          "dsa_read_device_status")
+    return int(v.value)
+
+
+def last_device_status(stream=None) -> int:
+    v = _lib.ctypes.c_int32(0)
+    check(_lib.load().dsa_last_device_status(_lib.ctypes.byref(v), _stream(stream)), "dsa_last_device_status")
+    return int(v.value)
+
+
+# ----------------------------------------------------------------------------------------
+# Workload conveniences (a workloads.Workload holds the tensors and the scalars).
+# ----------------------------------------------------------------------------------------
+
+def _workload_args(w):
+    vc = w.k_cache if w.v_cache is None else w.v_cache
+    return (w.q, w.k_cache, vc, w.block_tables, w.max_blocks_per_seq)
+
+
+def decode_workload(w, out=None, workspace=None, num_ctas=0, verify=None, stream=None, ev_begin=None,
+                    ev_end=None) -> torch.Tensor:
+    """Run the decode on a Workload. verify=True uses the k-row entry point with the
+    workload's per-sequence base lengths."""
+    q, kc, vc, bt, mbps = _workload_args(w)
+    out = torch.empty_like(q) if out is None else out
+    verify = (w.base_lens is not None) if verify is None else verify
+    lens = w.base_lens if verify else w.seq_lens
+    if workspace is None:
+        fn = decode_k if verify else decode
+        return fn(q, kc, vc, bt, mbps, lens, w.sel_indices, w.num_seqs, w.rows_per_seq, w.num_q_heads,
+                  w.block_size, w.cache_stride_bytes, w.k_scale, w.v_scale, w.sm_scale, out=out, stream=stream)
+    return decode_ws(q, kc, vc, bt, mbps, lens, w.sel_indices, w.num_seqs, w.rows_per_seq, w.num_q_heads,
+                     w.block_size, w.cache_stride_bytes, w.k_scale, w.v_scale, w.sm_scale, out, workspace,
+                     verify_rows=1 if verify else 0, num_ctas=num_ctas, ev_begin=ev_begin, ev_end=ev_end,
+                     stream=stream)

@@ -1,0 +1,450 @@
+// Host side of the C ABI declared in include/dsa_mla.h: argument checks, the work
+// partition, workspace management and the launch sequence
+//   prologue (index resolution + query split) -> decode -> combine (when needed),
+// all enqueued on the caller's stream.
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+
+using namespace dsa;
+
+namespace {
+
+struct DeviceState {
+    bool checked = false;
+    int32_t status = DSA_OK;  // result of the device check
+    int sms = 0;
+    void* ws = nullptr;       // library-owned workspace
+    size_t ws_bytes = 0;
+};
+
+std::mutex g_mu;
+std::vector<DeviceState> g_devices;
+
+struct Args {
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;
+    const int32_t* block_tables;
+    int32_t max_blocks_per_seq;
+    const int32_t* seq_lens;
+    const int32_t* sel;
+    int32_t width, num_seqs, rows_per_seq, heads, block_size;
+    int64_t stride;
+    float k_scale, v_scale, sm_scale;
+    void* out;
+    int32_t verify_rows;
+};
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int32_t check_args(const Args& a) {
+    if (!a.q || !a.k_cache || !a.v_cache || !a.block_tables || !a.seq_lens || !a.sel || !a.out)
+        return DSA_ERR_INVALID_ARGUMENT;
+    if (a.num_seqs < 1 || a.rows_per_seq < 1 || a.heads < 1 || a.block_size < 1 || a.width < 1 ||
+        a.max_blocks_per_seq < 0)
+        return DSA_ERR_INVALID_ARGUMENT;
+    if (a.stride < static_cast<int64_t>(a.block_size) * kLatent || a.stride % 16 != 0)
+        return DSA_ERR_INVALID_ARGUMENT;
+    if (!aligned(a.q, 16) || !aligned(a.out, 16) || !aligned(a.k_cache, 16) || !aligned(a.v_cache, 16) ||
+        !aligned(a.block_tables, 4) || !aligned(a.seq_lens, 4) || !aligned(a.sel, 4))
+        return DSA_ERR_INVALID_ARGUMENT;
+    if (a.verify_rows != 0 && a.verify_rows != 1) return DSA_ERR_INVALID_ARGUMENT;
+    const int64_t rows = static_cast<int64_t>(a.num_seqs) * a.rows_per_seq;
+    if (a.width > DSA_MAX_SEL_WIDTH) return DSA_ERR_UNSUPPORTED;
+    if (rows > (1LL << 30) / a.width || rows * a.heads > (1LL << 31) / kLatent) return DSA_ERR_UNSUPPORTED;
+    return DSA_OK;
+}
+
+int32_t from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return DSA_OK;
+    if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction ||
+        e == cudaErrorSharedObjectInitFailed)
+        return DSA_ERR_NO_KERNEL;
+    return DSA_ERR_CUDA;
+}
+
+// Checks the current device once (sm_103, kernels loadable) and returns its state.
+int32_t current_device(DeviceState** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DSA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (static_cast<int>(g_devices.size()) <= dev) g_devices.resize(dev + 1);
+    DeviceState& d = g_devices[dev];
+    if (!d.checked) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return DSA_ERR_CUDA;
+        d.sms = sms;
+        if (major != 10 || minor != 3) {
+            d.status = DSA_ERR_UNSUPPORTED;
+        } else {
+            d.status = from_cuda(decode_kernel_setup());
+            if (d.status == DSA_OK) d.status = from_cuda(prologue_kernel_setup());
+            if (d.status == DSA_OK) d.status = from_cuda(combine_kernel_setup());
+        }
+        d.checked = true;
+    }
+    *out = &d;
+    return d.status;
+}
+
+struct Plan {
+    int64_t rows, groups, units;
+    Partition part;
+    bool any_split;
+    WsLayout ws;
+};
+
+Plan make_plan(int64_t rows, int32_t heads, int32_t width, int32_t num_ctas, int sms) {
+    Plan pl;
+    pl.rows = rows;
+    pl.groups = (heads + kHeadsPerCta - 1) / kHeadsPerCta;
+    pl.units = rows * pl.groups;
+    pl.part.total_slots = pl.units * width;
+    pl.part.width = width;
+    pl.part.groups = static_cast<int32_t>(pl.groups);
+    int64_t c = num_ctas;
+    if (c <= 0) {
+        c = (pl.part.total_slots + kTileTokens - 1) / kTileTokens;
+        if (c > sms) c = sms;
+        if (c < 1) c = 1;
+    }
+    pl.part.ctas = static_cast<int32_t>(c);
+    pl.any_split = false;
+    for (int64_t k = 1; k < c && !pl.any_split; ++k)
+        if (cta_begin(pl.part, k) % width != 0) pl.any_split = true;
+    pl.ws = ws_layout(rows, pl.groups, width, c);
+    return pl;
+}
+
+int32_t enqueue(const Args& a, const Plan& pl, uint8_t* ws, cudaEvent_t ev0, cudaEvent_t ev1,
+                cudaStream_t stream) {
+    PrologueParams pp{};
+    pp.sel = a.sel;
+    pp.seq_lens = a.seq_lens;
+    pp.q = static_cast<const uint16_t*>(a.q);
+    pp.ids = reinterpret_cast<int32_t*>(ws + pl.ws.ids);
+    pp.cnt = reinterpret_cast<int32_t*>(ws + pl.ws.cnt);
+    pp.qimg = ws + pl.ws.qimg;
+    pp.qscale = reinterpret_cast<float*>(ws + pl.ws.qscale);
+    pp.status = reinterpret_cast<int*>(ws + pl.ws.status);
+    pp.rows = static_cast<int32_t>(pl.rows);
+    pp.width = a.width;
+    pp.heads = a.heads;
+    pp.groups = static_cast<int32_t>(pl.groups);
+    pp.rows_per_seq = a.rows_per_seq;
+    pp.verify_rows = a.verify_rows;
+    pp.score_scale = a.sm_scale * a.k_scale * 1.4426950408889634f;
+    int32_t st = from_cuda(launch_prologue(pp, static_cast<int>(pl.rows + pl.units), stream));
+    if (st != DSA_OK) return st;
+
+    DecodeParams dp{};
+    dp.k_cache = static_cast<const uint8_t*>(a.k_cache);
+    dp.v_cache = static_cast<const uint8_t*>(a.v_cache);
+    dp.block_tables = a.block_tables;
+    dp.ids = pp.ids;
+    dp.cnt = pp.cnt;
+    dp.qimg = pp.qimg;
+    dp.qscale = pp.qscale;
+    dp.out = static_cast<uint16_t*>(a.out);
+    dp.part_o = reinterpret_cast<float*>(ws + pl.ws.part_o);
+    dp.part_lse = reinterpret_cast<float*>(ws + pl.ws.part_lse);
+    dp.status = pp.status;
+    dp.cache_stride = a.stride;
+    dp.part = pl.part;
+    dp.heads = a.heads;
+    dp.rows_per_seq = a.rows_per_seq;
+    dp.block_size = a.block_size;
+    dp.block_shift = -1;
+    for (int s = 0; s < 31; ++s)
+        if ((1 << s) == a.block_size) dp.block_shift = s;
+    dp.max_blocks_per_seq = a.max_blocks_per_seq;
+    dp.kv_same = a.k_cache == a.v_cache ? 1 : 0;
+    dp.v_scale = a.v_scale;
+    if (ev0 && cudaEventRecord(ev0, stream) != cudaSuccess) return DSA_ERR_CUDA;
+    st = from_cuda(launch_decode(dp, stream));
+    if (st != DSA_OK) return st;
+    if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess) return DSA_ERR_CUDA;
+
+    if (pl.any_split) {
+        CombineParams cp{};
+        cp.part_o = dp.part_o;
+        cp.part_lse = dp.part_lse;
+        cp.out = dp.out;
+        cp.part = pl.part;
+        cp.heads = a.heads;
+        cp.v_scale = a.v_scale;
+        st = from_cuda(launch_combine(cp, static_cast<int>(pl.units), stream));
+    }
+    return st;
+}
+
+int32_t run_ws(const Args& a, void* workspace, size_t workspace_bytes, int32_t num_ctas, cudaEvent_t ev0,
+               cudaEvent_t ev1, cudaStream_t stream) {
+    int32_t st = check_args(a);
+    if (st != DSA_OK) return st;
+    if (!workspace || !aligned(workspace, 256) || num_ctas < 0) return DSA_ERR_INVALID_ARGUMENT;
+    DeviceState* d = nullptr;
+    st = current_device(&d);
+    if (st != DSA_OK) return st;
+    const Plan pl = make_plan(static_cast<int64_t>(a.num_seqs) * a.rows_per_seq, a.heads, a.width, num_ctas, d->sms);
+    if (workspace_bytes < pl.ws.total) return DSA_ERR_WORKSPACE;
+    return enqueue(a, pl, static_cast<uint8_t*>(workspace), ev0, ev1, stream);
+}
+
+int32_t run_lib(const Args& a, cudaStream_t stream) {
+    int32_t st = check_args(a);
+    if (st != DSA_OK) return st;
+    DeviceState* d = nullptr;
+    st = current_device(&d);
+    if (st != DSA_OK) return st;
+    const Plan pl = make_plan(static_cast<int64_t>(a.num_seqs) * a.rows_per_seq, a.heads, a.width, 0, d->sms);
+    void* ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (d->ws_bytes < pl.ws.total) {
+            cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+            if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return DSA_ERR_CUDA;
+            if (cs != cudaStreamCaptureStatusNone) return DSA_ERR_WORKSPACE;
+            if (d->ws) {
+                if (cudaStreamSynchronize(stream) != cudaSuccess) return DSA_ERR_CUDA;
+                cudaFree(d->ws);
+                d->ws = nullptr;
+                d->ws_bytes = 0;
+            }
+            const size_t want = pl.ws.total + pl.ws.total / 4;
+            if (cudaMalloc(&d->ws, want) != cudaSuccess) return DSA_ERR_CUDA;
+            if (cudaMemset(d->ws, 0, 256) != cudaSuccess) return DSA_ERR_CUDA;
+            d->ws_bytes = want;
+        }
+        ws = d->ws;
+    }
+    return enqueue(a, pl, static_cast<uint8_t*>(ws), nullptr, nullptr, stream);
+}
+
+Args make_args(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+               int32_t max_blocks_per_seq, const int32_t* seq_lens, const int32_t* sel, int32_t width,
+               int32_t num_seqs, int32_t rows_per_seq, int32_t heads, int32_t block_size, int64_t stride,
+               float k_scale, float v_scale, float sm_scale, void* out, int32_t verify_rows) {
+    Args a;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.seq_lens = seq_lens;
+    a.sel = sel;
+    a.width = width;
+    a.num_seqs = num_seqs;
+    a.rows_per_seq = rows_per_seq;
+    a.heads = heads;
+    a.block_size = block_size;
+    a.stride = stride;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.sm_scale = sm_scale;
+    a.out = out;
+    a.verify_rows = verify_rows;
+    return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t dsa_abi_version(void) { return 1; }
+
+const char* dsa_status_string(int32_t status) {
+    switch (status) {
+        case DSA_OK: return "ok";
+        case DSA_ERR_INVALID_ARGUMENT: return "invalid argument";
+        case DSA_ERR_UNSUPPORTED: return "unsupported device or size";
+        case DSA_ERR_WORKSPACE: return "workspace too small or growth during graph capture";
+        case DSA_ERR_CUDA: return "CUDA runtime error";
+        case DSA_ERR_NO_KERNEL: return "sm_103a kernel image missing for this device";
+        case DSA_ERR_DEVICE_BOUNDS: return "device: page lookup outside the block table";
+        case DSA_ERR_TIMEOUT: return "device: pipeline wait timed out";
+        default: return "unknown status";
+    }
+}
+
+int32_t dsa_mla_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                       int32_t max_blocks_per_seq, const int32_t* seq_lens, const int32_t* sel_indices,
+                       int32_t sel_width, int32_t num_seqs, int32_t rows_per_seq, int32_t num_q_heads,
+                       int32_t block_size, int64_t cache_stride_bytes, float k_scale, float v_scale,
+                       float sm_scale, void* out, void* stream) {
+    return run_lib(make_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, sel_indices,
+                             sel_width, num_seqs, rows_per_seq, num_q_heads, block_size, cache_stride_bytes,
+                             k_scale, v_scale, sm_scale, out, 0),
+                   static_cast<cudaStream_t>(stream));
+}
+
+int32_t dsa_mla_decode_k(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                         int32_t max_blocks_per_seq, const int32_t* seq_lens, const int32_t* sel_indices,
+                         int32_t sel_width, int32_t num_seqs, int32_t k, int32_t num_q_heads, int32_t block_size,
+                         int64_t cache_stride_bytes, float k_scale, float v_scale, float sm_scale, void* out,
+                         void* stream) {
+    return run_lib(make_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, sel_indices,
+                             sel_width, num_seqs, k, num_q_heads, block_size, cache_stride_bytes, k_scale,
+                             v_scale, sm_scale, out, 1),
+                   static_cast<cudaStream_t>(stream));
+}
+
+size_t dsa_mla_decode_workspace_bytes(int32_t num_seqs, int32_t rows_per_seq, int32_t num_q_heads,
+                                      int32_t sel_width, int32_t num_ctas) {
+    if (num_seqs < 1 || rows_per_seq < 1 || num_q_heads < 1 || sel_width < 1 || num_ctas < 0) return 0;
+    int sms = 0;
+    if (num_ctas == 0) {
+        DeviceState* d = nullptr;
+        if (current_device(&d) != DSA_OK) return 0;
+        sms = d->sms;
+    }
+    return make_plan(static_cast<int64_t>(num_seqs) * rows_per_seq, num_q_heads, sel_width, num_ctas, sms).ws.total;
+}
+
+int32_t dsa_mla_decode_ws(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                          int32_t max_blocks_per_seq, const int32_t* seq_lens, const int32_t* sel_indices,
+                          int32_t sel_width, int32_t num_seqs, int32_t rows_per_seq, int32_t num_q_heads,
+                          int32_t block_size, int64_t cache_stride_bytes, float k_scale, float v_scale,
+                          float sm_scale, void* out, int32_t verify_rows, void* workspace, size_t workspace_bytes,
+                          int32_t num_ctas, void* ev_begin, void* ev_end, void* stream) {
+    return run_ws(make_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, sel_indices,
+                            sel_width, num_seqs, rows_per_seq, num_q_heads, block_size, cache_stride_bytes,
+                            k_scale, v_scale, sm_scale, out, verify_rows),
+                  workspace, workspace_bytes, num_ctas, static_cast<cudaEvent_t>(ev_begin),
+                  static_cast<cudaEvent_t>(ev_end), static_cast<cudaStream_t>(stream));
+}
+
+namespace {
+struct HostStaging {
+    size_t q, bt, sl, sel, out, total;
+};
+HostStaging host_staging(size_t base, int64_t rows, int32_t heads, int32_t width, int32_t table_rows,
+                         int32_t mbps, int32_t num_seqs, int32_t verify_rows) {
+    HostStaging h;
+    size_t o = align256(base);
+    h.q = o; o = align256(o + static_cast<size_t>(rows) * heads * kLatent * 2);
+    h.bt = o; o = align256(o + static_cast<size_t>(table_rows) * (mbps > 0 ? mbps : 1) * 4);
+    h.sl = o; o = align256(o + static_cast<size_t>(verify_rows ? num_seqs : rows) * 4);
+    h.sel = o; o = align256(o + static_cast<size_t>(rows) * width * 4);
+    h.out = o; o = align256(o + static_cast<size_t>(rows) * heads * kLatent * 2);
+    h.total = o;
+    return h;
+}
+}  // namespace
+
+size_t dsa_mla_decode_host_workspace_bytes(int32_t num_seqs, int32_t rows_per_seq, int32_t num_q_heads,
+                                           int32_t sel_width, int32_t table_rows, int32_t max_blocks_per_seq,
+                                           int32_t verify_rows, int32_t num_ctas) {
+    const size_t base = dsa_mla_decode_workspace_bytes(num_seqs, rows_per_seq, num_q_heads, sel_width, num_ctas);
+    if (base == 0 || table_rows < 1 || max_blocks_per_seq < 0) return 0;
+    return host_staging(base, static_cast<int64_t>(num_seqs) * rows_per_seq, num_q_heads, sel_width, table_rows,
+                        max_blocks_per_seq, num_seqs, verify_rows)
+        .total;
+}
+
+int32_t dsa_mla_decode_host(const void* q_host, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables_host, int32_t table_rows, int32_t max_blocks_per_seq,
+                            const int32_t* seq_lens_host, const int32_t* sel_indices_host, int32_t sel_width,
+                            int32_t num_seqs, int32_t rows_per_seq, int32_t num_q_heads, int32_t block_size,
+                            int64_t cache_stride_bytes, float k_scale, float v_scale, float sm_scale,
+                            void* out_host, int32_t verify_rows, void* workspace, size_t workspace_bytes,
+                            int32_t num_ctas, void* stream) {
+    if (!q_host || !block_tables_host || !seq_lens_host || !sel_indices_host || !out_host || table_rows < 1 ||
+        !workspace || !aligned(workspace, 256))
+        return DSA_ERR_INVALID_ARGUMENT;
+    // Validate the shape with the device staging pointers standing in for the host ones.
+    Args probe = make_args(workspace, k_cache, v_cache, reinterpret_cast<const int32_t*>(workspace),
+                           max_blocks_per_seq, reinterpret_cast<const int32_t*>(workspace),
+                           reinterpret_cast<const int32_t*>(workspace), sel_width, num_seqs, rows_per_seq,
+                           num_q_heads, block_size, cache_stride_bytes, k_scale, v_scale, sm_scale, workspace,
+                           verify_rows);
+    int32_t st = check_args(probe);
+    if (st != DSA_OK) return st;
+    DeviceState* d = nullptr;
+    st = current_device(&d);
+    if (st != DSA_OK) return st;
+    const int64_t rows = static_cast<int64_t>(num_seqs) * rows_per_seq;
+    const Plan pl = make_plan(rows, num_q_heads, sel_width, num_ctas, d->sms);
+    const HostStaging hs = host_staging(pl.ws.total, rows, num_q_heads, sel_width, table_rows, max_blocks_per_seq,
+                                        num_seqs, verify_rows);
+    if (workspace_bytes < hs.total) return DSA_ERR_WORKSPACE;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t qb = static_cast<size_t>(rows) * num_q_heads * kLatent * 2;
+    const size_t btb = static_cast<size_t>(table_rows) * (max_blocks_per_seq > 0 ? max_blocks_per_seq : 1) * 4;
+    const size_t slb = static_cast<size_t>(verify_rows ? num_seqs : rows) * 4;
+    const size_t selb = static_cast<size_t>(rows) * sel_width * 4;
+    if (cudaMemcpyAsync(ws + hs.q, q_host, qb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(ws + hs.bt, block_tables_host, btb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(ws + hs.sl, seq_lens_host, slb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(ws + hs.sel, sel_indices_host, selb, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return DSA_ERR_CUDA;
+    Args a = make_args(ws + hs.q, k_cache, v_cache, reinterpret_cast<const int32_t*>(ws + hs.bt),
+                       max_blocks_per_seq, reinterpret_cast<const int32_t*>(ws + hs.sl),
+                       reinterpret_cast<const int32_t*>(ws + hs.sel), sel_width, num_seqs, rows_per_seq,
+                       num_q_heads, block_size, cache_stride_bytes, k_scale, v_scale, sm_scale, ws + hs.out,
+                       verify_rows);
+    st = enqueue(a, pl, ws, nullptr, nullptr, s);
+    if (st != DSA_OK) return st;
+    if (cudaMemcpyAsync(out_host, ws + hs.out, qb, cudaMemcpyDeviceToHost, s) != cudaSuccess) return DSA_ERR_CUDA;
+    return DSA_OK;
+}
+
+int32_t dsa_resolve_indices(const int32_t* sel_indices, const int32_t* seq_lens, int32_t sel_width, int32_t rows,
+                            int32_t* ids_out, int32_t* counts_out, void* stream) {
+    if (!sel_indices || !seq_lens || !ids_out || !counts_out || sel_width < 1 || rows < 1)
+        return DSA_ERR_INVALID_ARGUMENT;
+    if (!aligned(sel_indices, 4) || !aligned(seq_lens, 4) || !aligned(ids_out, 4) || !aligned(counts_out, 4))
+        return DSA_ERR_INVALID_ARGUMENT;
+    if (sel_width > DSA_MAX_SEL_WIDTH) return DSA_ERR_UNSUPPORTED;
+    DeviceState* d = nullptr;
+    int32_t st = current_device(&d);
+    if (st != DSA_OK) return st;
+    PrologueParams pp{};
+    pp.sel = sel_indices;
+    pp.seq_lens = seq_lens;
+    pp.ids = ids_out;
+    pp.cnt = counts_out;
+    pp.rows = rows;
+    pp.width = sel_width;
+    pp.heads = 1;
+    pp.groups = 1;
+    pp.rows_per_seq = 1;
+    return from_cuda(launch_prologue(pp, rows, static_cast<cudaStream_t>(stream)));
+}
+
+int32_t dsa_read_device_status(const void* workspace, int32_t* status_out, void* stream) {
+    if (!workspace || !status_out) return DSA_ERR_INVALID_ARGUMENT;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return DSA_ERR_CUDA;
+    *status_out = v;
+    return DSA_OK;
+}
+
+int32_t dsa_last_device_status(int32_t* status_out, void* stream) {
+    if (!status_out) return DSA_ERR_INVALID_ARGUMENT;
+    DeviceState* d = nullptr;
+    int32_t st = current_device(&d);
+    if (st != DSA_OK) return st;
+    void* ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        ws = d->ws;
+    }
+    if (!ws) {
+        *status_out = DSA_OK;
+        return DSA_OK;
+    }
+    return dsa_read_device_status(ws, status_out, stream);
+}
+
+}  // extern "C"

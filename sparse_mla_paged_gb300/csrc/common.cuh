@@ -1,0 +1,161 @@
+// Shared definitions of the decode library: tile geometry, kernel parameter blocks,
+// workspace layout and the static work partition. Host and device code both use the
+// partition helpers, so the decode kernel and the combine kernel agree on it exactly.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "dsa_mla.h"
+
+namespace dsa {
+
+constexpr int kLatent = 512;           // kv_lora_rank: the whole cache token (NoPE)
+constexpr int kTileTokens = 128;       // tokens per tile = MMA M of the score product
+constexpr int kHeadsPerCta = 64;       // query heads per work unit
+constexpr int kQImageBytes = 2 * kHeadsPerCta * kLatent;  // E4M3 hi + lo terms, 64 KB
+constexpr int kKvTileBytes = kTileTokens * kLatent;       // 64 KB of E4M3 per tile
+constexpr int kKBlockBytes = kTileTokens * 128;           // one 128-dim slab of a tile
+constexpr int kBitmapWords = 8192;     // resolve bitmap: seq_len up to 262144 tokens
+constexpr int kResolveThreads = 256;
+
+// Score-probability scaling: P' = 256 * exp2(x - m) lies in [0, 256] and is carried as
+// two E4M3 terms (see decode.cu).
+constexpr float kPScale = 256.0f;
+
+// Device status codes mirror dsa_status.
+constexpr int kStatusBounds = DSA_ERR_DEVICE_BOUNDS;
+constexpr int kStatusTimeout = DSA_ERR_TIMEOUT;
+
+// ------------------------------------------------------------------------------------
+// Workspace layout (all offsets 256-byte aligned).
+// ------------------------------------------------------------------------------------
+struct WsLayout {
+    size_t status, ids, cnt, qimg, qscale, part_o, part_lse, total;
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+__host__ __device__ inline WsLayout ws_layout(int64_t rows, int64_t groups, int64_t width, int64_t ctas) {
+    WsLayout L;
+    size_t o = 0;
+    L.status = o; o += 256;
+    L.ids = o; o = align256(o + static_cast<size_t>(rows * width) * 4);
+    L.cnt = o; o = align256(o + static_cast<size_t>(rows) * 4);
+    L.qimg = o; o = align256(o + static_cast<size_t>(rows * groups) * kQImageBytes);
+    L.qscale = o; o = align256(o + static_cast<size_t>(rows * groups) * kHeadsPerCta * 4);
+    L.part_o = o; o = align256(o + static_cast<size_t>(2 * ctas) * kHeadsPerCta * kLatent * 4);
+    L.part_lse = o; o = align256(o + static_cast<size_t>(2 * ctas) * kHeadsPerCta * 4);
+    L.total = o;
+    return L;
+}
+
+// ------------------------------------------------------------------------------------
+// Static work partition.
+//
+// A work unit is (row r, head group g) with sel_width "slots"; units are ordered
+// u = r*groups + g. The concatenated slot space [0, T), T = units*sel_width, is cut into
+// num_ctas contiguous ranges [c*T/C, (c+1)*T/C). A unit's slot range [s0, s1) maps to
+// resolved-token range [s0*U/W, s1*U/W) of that row (U = resolved count), so ranges of
+// neighbouring CTAs abut exactly whatever U is. A unit covered by one CTA is written
+// straight to the output; a unit shared by several CTAs leaves per-CTA partials (slot
+// 2c for the CTA's first unit, 2c+1 for its last) that the combine kernel merges.
+// ------------------------------------------------------------------------------------
+struct Partition {
+    int64_t total_slots;  // T
+    int32_t width;        // W
+    int32_t ctas;         // C
+    int32_t groups;       // G
+};
+
+__host__ __device__ inline int64_t cta_begin(const Partition& p, int64_t c) {
+    return c * p.total_slots / p.ctas;
+}
+// The CTA whose range holds slot x (the last one starting at or before x).
+__host__ __device__ inline int64_t cta_of_slot(const Partition& p, int64_t x) {
+    return ((x + 1) * p.ctas - 1) / p.total_slots;
+}
+
+struct Segment {
+    int32_t unit, row, group;
+    int64_t s0, s1;     // slot range within the unit
+    int32_t part;       // partial slot, -1 when this CTA owns the whole unit
+};
+
+// Number of segments (units touched) of CTA c.
+__host__ __device__ inline int32_t cta_segments(const Partition& p, int64_t c, int64_t* first_unit) {
+    const int64_t b = cta_begin(p, c), e = cta_begin(p, c + 1);
+    *first_unit = b / p.width;
+    if (e <= b) return 0;
+    return static_cast<int32_t>((e - 1) / p.width - b / p.width + 1);
+}
+
+__host__ __device__ inline Segment cta_segment(const Partition& p, int64_t c, int32_t i) {
+    const int64_t b = cta_begin(p, c), e = cta_begin(p, c + 1);
+    const int64_t u = b / p.width + i;
+    Segment s;
+    s.unit = static_cast<int32_t>(u);
+    s.row = static_cast<int32_t>(u / p.groups);
+    s.group = static_cast<int32_t>(u % p.groups);
+    const int64_t ub = u * p.width;
+    s.s0 = (b > ub ? b : ub) - ub;
+    s.s1 = (e < ub + p.width ? e : ub + p.width) - ub;
+    const bool whole = (s.s0 == 0 && s.s1 == p.width);
+    s.part = whole ? -1 : static_cast<int32_t>(2 * c + (i == 0 ? 0 : 1));
+    return s;
+}
+
+// ------------------------------------------------------------------------------------
+// Kernel parameter blocks.
+// ------------------------------------------------------------------------------------
+struct PrologueParams {
+    const int32_t* sel;        // [R, W]
+    const int32_t* seq_lens;   // [R] or [num_seqs] (verify rows)
+    const uint16_t* q;         // bf16 bits [R, H, 512]; null: resolve only
+    int32_t* ids;              // [R, W]
+    int32_t* cnt;              // [R]
+    uint8_t* qimg;             // [R*G, 64 KB]
+    float* qscale;             // [R*G, 64]
+    int* status;               // reset by block 0 (may be null)
+    int32_t rows, width, heads, groups, rows_per_seq, verify_rows;
+    float score_scale;         // sm_scale * k_scale * log2(e)
+};
+
+struct DecodeParams {
+    const uint8_t* k_cache;
+    const uint8_t* v_cache;
+    const int32_t* block_tables;
+    const int32_t* ids;
+    const int32_t* cnt;
+    const uint8_t* qimg;
+    const float* qscale;
+    uint16_t* out;             // bf16 bits [R, H, 512]
+    float* part_o;             // [2C, 64, 512]
+    float* part_lse;           // [2C, 64]
+    int* status;
+    int64_t cache_stride;
+    Partition part;
+    int32_t heads, rows_per_seq, block_size, block_shift, max_blocks_per_seq;
+    int32_t kv_same;
+    float v_scale;
+};
+
+struct CombineParams {
+    const float* part_o;
+    const float* part_lse;
+    uint16_t* out;
+    Partition part;
+    int32_t heads;
+    float v_scale;
+};
+
+// Launchers (each defined next to its kernel).
+cudaError_t launch_prologue(const PrologueParams& p, int blocks, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_combine(const CombineParams& p, int units, cudaStream_t stream);
+cudaError_t decode_kernel_setup();
+cudaError_t prologue_kernel_setup();
+cudaError_t combine_kernel_setup();
+
+}  // namespace dsa

@@ -1,0 +1,208 @@
+// Prologue of the decode: index resolution and query preparation, one launch.
+//
+// Blocks [0, rows) resolve one selection row each (attend.rs module doc: -1 holes,
+// set membership with duplicates collapsed; decode_k.rs: row r only sees positions
+// below its own seq_len): the distinct ids 0 <= id < L in ascending order, -1 padded.
+//   * L <= 262144: a bitmap of L bits in shared memory; ids set with atomicOr and
+//     written out by a block-wide prefix count, which yields them sorted.
+//   * longer rows: bitonic sort of the row in shared memory, then a prefix count of
+//     first occurrences.
+// Blocks [rows, rows + rows*groups) turn one (row, 64-head group) of BF16 queries into
+// the shared-memory image the decode kernel copies verbatim: per head a power-of-two
+// scale 2^e (|q|*2^e < 256) and two E4M3 terms hi + lo whose sum is q*2^e. hi keeps the
+// top 4 significant bits (truncation), lo is the remainder; for |q*2^e| >= 2^-2 the
+// split is exact, since a BF16 value has 8 significant bits. Rows 0..63 of the image
+// hold hi, rows 64..127 lo, in the K-major 128-byte-swizzled operand layout.
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace dsa {
+namespace {
+
+__device__ __forceinline__ int32_t row_seq_len(const PrologueParams& p, int32_t r) {
+    int32_t L = p.verify_rows ? p.seq_lens[r / p.rows_per_seq] + (r % p.rows_per_seq) + 1 : p.seq_lens[r];
+    return L < 0 ? 0 : L;
+}
+
+// Exclusive prefix sum over the block (kResolveThreads threads); also returns the total.
+__device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t* scratch, int32_t* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int32_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) scratch[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int32_t w = lane < kResolveThreads / 32 ? scratch[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int32_t y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        if (lane < kResolveThreads / 32) scratch[lane] = w;  // inclusive per-warp totals
+    }
+    __syncthreads();
+    const int32_t before = (warp > 0 ? scratch[warp - 1] : 0) + x - v;
+    *total = scratch[kResolveThreads / 32 - 1];
+    __syncthreads();
+    return before;
+}
+
+__device__ void resolve_row(const PrologueParams& p, int32_t r, uint32_t* sm, int32_t* scratch) {
+    const int tid = threadIdx.x;
+    const int32_t W = p.width;
+    const int32_t L = row_seq_len(p, r);
+    const int32_t* sel = p.sel + static_cast<int64_t>(r) * W;
+    int32_t* ids = p.ids + static_cast<int64_t>(r) * W;
+    int32_t total = 0;
+    if (L <= kBitmapWords * 32) {
+        const int32_t nwords = (L + 31) >> 5;
+        for (int32_t w = tid; w < nwords; w += kResolveThreads) sm[w] = 0u;
+        __syncthreads();
+        for (int32_t j = tid; j < W; j += kResolveThreads) {
+            const int32_t id = sel[j];
+            if (id >= 0 && id < L) atomicOr(&sm[id >> 5], 1u << (id & 31));
+        }
+        __syncthreads();
+        const int32_t per = (nwords + kResolveThreads - 1) / kResolveThreads;
+        const int32_t w0 = tid * per;
+        const int32_t w1 = min(w0 + per, nwords);
+        int32_t mine = 0;
+        for (int32_t w = w0; w < w1; ++w) mine += __popc(sm[w]);
+        int32_t pos = block_exclusive_scan(mine, scratch, &total);
+        for (int32_t w = w0; w < w1; ++w) {
+            uint32_t bits = sm[w];
+            while (bits) {
+                const int b = __ffs(bits) - 1;
+                ids[pos++] = w * 32 + b;
+                bits &= bits - 1;
+            }
+        }
+    } else {
+        int32_t* keys = reinterpret_cast<int32_t*>(sm);
+        int32_t n = 1;
+        while (n < W) n <<= 1;
+        for (int32_t j = tid; j < n; j += kResolveThreads) {
+            int32_t id = j < W ? sel[j] : -1;
+            keys[j] = (id >= 0 && id < L) ? id : INT32_MAX;
+        }
+        __syncthreads();
+        for (int32_t k = 2; k <= n; k <<= 1) {
+            for (int32_t j = k >> 1; j > 0; j >>= 1) {
+                for (int32_t i = tid; i < n; i += kResolveThreads) {
+                    const int32_t x = i ^ j;
+                    if (x > i) {
+                        const int32_t a = keys[i], b = keys[x];
+                        const bool up = (i & k) == 0;
+                        if ((a > b) == up) {
+                            keys[i] = b;
+                            keys[x] = a;
+                        }
+                    }
+                }
+                __syncthreads();
+            }
+        }
+        const int32_t per = (W + kResolveThreads - 1) / kResolveThreads;
+        const int32_t j0 = tid * per;
+        const int32_t j1 = min(j0 + per, W);
+        int32_t mine = 0;
+        for (int32_t j = j0; j < j1; ++j)
+            mine += (keys[j] != INT32_MAX && (j == 0 || keys[j] != keys[j - 1])) ? 1 : 0;
+        int32_t pos = block_exclusive_scan(mine, scratch, &total);
+        for (int32_t j = j0; j < j1; ++j)
+            if (keys[j] != INT32_MAX && (j == 0 || keys[j] != keys[j - 1])) ids[pos++] = keys[j];
+    }
+    for (int32_t j = total + tid; j < W; j += kResolveThreads) ids[j] = -1;
+    if (tid == 0) p.cnt[r] = total;
+}
+
+// One (row, group): 8 warps x 8 heads; lane l handles latent dims [16l, 16l+16).
+__device__ void prepare_queries(const PrologueParams& p, int32_t unit) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int32_t r = unit / p.groups, g = unit % p.groups;
+    uint8_t* img = p.qimg + static_cast<int64_t>(unit) * kQImageBytes;
+    for (int hl = warp; hl < kHeadsPerCta; hl += kResolveThreads / 32) {
+        const int32_t h = g * kHeadsPerCta + hl;
+        float x[16];
+        if (h < p.heads) {
+            const uint4* src = reinterpret_cast<const uint4*>(
+                p.q + (static_cast<int64_t>(r) * p.heads + h) * kLatent + lane * 16);
+            const uint4 a = src[0], b = src[1];
+            const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                x[2 * i] = __uint_as_float(w[i] << 16);
+                x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) x[i] = 0.0f;
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        // e with amax * 2^e in [128, 256): amax = 1.m * 2^(E-127), so e = 134 - E.
+        int e = 0;
+        if (amax > 0.0f) {
+            const int E = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF);
+            e = 134 - E;
+            e = e > 126 ? 126 : (e < -126 ? -126 : e);
+        }
+        const float s = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float v[4], vh[4], vl[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                v[k] = x[4 * i + k] * s;
+                vh[k] = __uint_as_float(__float_as_uint(v[k]) & 0xFFF00000u);
+                vl[k] = v[k] - vh[k];
+            }
+            hi[i] = f32x2_to_e4m3x2(vh[0], vh[1]) | (f32x2_to_e4m3x2(vh[2], vh[3]) << 16);
+            lo[i] = f32x2_to_e4m3x2(vl[0], vl[1]) | (f32x2_to_e4m3x2(vl[2], vl[3]) << 16);
+        }
+        // K-major SW128 image: K-block kb = lane/8 (128 dims), 16-byte chunk c = lane%8,
+        // row j stored at kb*16K + j*128 with its chunks permuted by j%8.
+        const int kb = lane >> 3, c = lane & 7;
+        const int jh = hl, jl = kHeadsPerCta + hl;
+        *reinterpret_cast<uint4*>(img + kb * kKBlockBytes + jh * 128 + ((c ^ (jh & 7)) << 4)) =
+            make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(img + kb * kKBlockBytes + jl * 128 + ((c ^ (jl & 7)) << 4)) =
+            make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        if (lane == 0)
+            p.qscale[static_cast<int64_t>(unit) * kHeadsPerCta + hl] =
+                p.score_scale * __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+    }
+}
+
+__global__ void __launch_bounds__(kResolveThreads) prologue_kernel(const PrologueParams p) {
+    extern __shared__ __align__(16) uint32_t bitmap[];
+    __shared__ int32_t scratch[kResolveThreads / 32];
+    if (blockIdx.x == 0 && threadIdx.x == 0 && p.status) *p.status = 0;
+    if (static_cast<int32_t>(blockIdx.x) < p.rows)
+        resolve_row(p, blockIdx.x, bitmap, scratch);
+    else
+        prepare_queries(p, blockIdx.x - p.rows);
+}
+
+}  // namespace
+
+cudaError_t prologue_kernel_setup() {
+    cudaFuncAttributes attr;
+    return cudaFuncGetAttributes(&attr, prologue_kernel);
+}
+
+cudaError_t launch_prologue(const PrologueParams& p, int blocks, cudaStream_t stream) {
+    if (blocks <= 0) return cudaSuccess;
+    prologue_kernel<<<blocks, kResolveThreads, kBitmapWords * 4, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace dsa

@@ -1,0 +1,99 @@
+"""C ABI checks that need no GPU: the library loads, exports every entry point the
+header declares with the signatures the binding uses, and rejects invalid arguments on
+the host before touching CUDA."""
+import ctypes
+import re
+
+import pytest
+
+from sparse_mla_paged_gb300 import _lib
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_mla_paged_gb300 import build
+    build.build()
+    return _lib.load()
+
+
+def _declared_functions():
+    text = open(_lib.HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_\w+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    names = _declared_functions()
+    for want in ("dsa_mla_decode", "dsa_mla_decode_k", "dsa_mla_decode_ws", "dsa_resolve_indices",
+                 "dsa_mla_decode_workspace_bytes", "dsa_status_string", "dsa_read_device_status",
+                 "dsa_mla_decode_host"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, f"{name} has no binding signature"
+
+
+def test_status_strings(lib):
+    assert lib.dsa_abi_version() == 1
+    for code, name in _lib.STATUS.items():
+        s = lib.dsa_status_string(code).decode()
+        assert s and s != "unknown status", name
+    assert lib.dsa_status_string(99).decode() == "unknown status"
+
+
+# A valid-looking argument set with fake, aligned device addresses; host-side checks
+# reject the variations below before any CUDA call is made.
+BASE = dict(q=0x10000, k=0x20000, v=0x20000, bt=0x30000, mbps=64, sl=0x40000, sel=0x50000, width=2048,
+            seqs=8, rps=1, heads=64, bs=64, stride=64 * 512, ks=0.05, vs=0.05, sm=0.044, out=0x60000)
+
+
+def _call(lib, **over):
+    a = dict(BASE, **over)
+    return lib.dsa_mla_decode(a["q"], a["k"], a["v"], a["bt"], a["mbps"], a["sl"], a["sel"], a["width"],
+                              a["seqs"], a["rps"], a["heads"], a["bs"], a["stride"], a["ks"], a["vs"], a["sm"],
+                              a["out"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=0), 1), (dict(k=0), 1), (dict(v=0), 1), (dict(bt=0), 1), (dict(sl=0), 1), (dict(sel=0), 1),
+    (dict(out=0), 1), (dict(seqs=0), 1), (dict(heads=0), 1), (dict(rps=0), 1), (dict(bs=0), 1),
+    (dict(width=0), 1), (dict(mbps=-1), 1), (dict(stride=64 * 512 - 16), 1), (dict(stride=64 * 512 + 8), 1),
+    (dict(q=0x10008), 1), (dict(out=0x60002), 1), (dict(k=0x20004), 1), (dict(bt=0x30002), 1),
+    (dict(width=8193), 2),
+])
+def test_invalid_arguments_rejected_on_host(lib, over, code):
+    assert _call(lib, **over) == code
+
+
+def test_decode_ws_rejects_bad_workspace_on_host(lib):
+    a = BASE
+    args = [a["q"], a["k"], a["v"], a["bt"], a["mbps"], a["sl"], a["sel"], a["width"], a["seqs"], a["rps"],
+            a["heads"], a["bs"], a["stride"], a["ks"], a["vs"], a["sm"], a["out"]]
+    assert lib.dsa_mla_decode_ws(*args, 0, None, 1 << 20, 0, None, None, None) == 1       # null workspace
+    assert lib.dsa_mla_decode_ws(*args, 0, 0x70010, 1 << 20, 0, None, None, None) == 1    # misaligned
+    assert lib.dsa_mla_decode_ws(*args, 2, 0x70000, 1 << 20, 0, None, None, None) == 1    # bad verify flag
+    assert lib.dsa_mla_decode_ws(*args, 0, 0x70000, 1 << 20, -1, None, None, None) == 1   # bad grid
+
+
+def test_resolve_rejects_bad_arguments_on_host(lib):
+    assert lib.dsa_resolve_indices(None, 0x1000, 8, 1, 0x2000, 0x3000, None) == 1
+    assert lib.dsa_resolve_indices(0x1000, 0x1000, 0, 1, 0x2000, 0x3000, None) == 1
+    assert lib.dsa_resolve_indices(0x1000, 0x1000, 8, 0, 0x2000, 0x3000, None) == 1
+    assert lib.dsa_resolve_indices(0x1002, 0x1000, 8, 1, 0x2000, 0x3000, None) == 1
+    assert lib.dsa_resolve_indices(0x1000, 0x1000, 9000, 1, 0x2000, 0x3000, None) == 2
+
+
+def test_workspace_size_grows_with_the_problem(lib):
+    f = lib.dsa_mla_decode_workspace_bytes
+    base = f(8, 1, 64, 2048, 152)
+    assert base > 0 and base % 256 == 0
+    assert f(16, 1, 64, 2048, 152) > base          # more rows
+    assert f(8, 1, 128, 2048, 152) > base          # second head group
+    assert f(8, 1, 64, 2048, 300) > base           # more partial slots
+    # at least ids + counts + query images + partials
+    rows, width, ctas = 8, 2048, 152
+    assert base >= rows * width * 4 + rows * 4 + rows * 65536 + 2 * ctas * 64 * 512 * 4
+    assert f(0, 1, 64, 2048, 152) == 0
