@@ -22,6 +22,9 @@ struct DeviceState {
 
 std::mutex g_mu;
 std::vector<DeviceState> g_devices;
+#ifdef DSA_TRACE
+unsigned long long* g_trace = nullptr;  // trace builds only: per-CTA decode timeline
+#endif
 
 struct Args {
     const void* q;
@@ -128,6 +131,14 @@ int32_t enqueue(const Args& a, const Plan& pl, uint8_t* ws, cudaEvent_t ev0, cud
     pp.sel = a.sel;
     pp.seq_lens = a.seq_lens;
     pp.q = static_cast<const uint16_t*>(a.q);
+    pp.block_tables = a.block_tables;
+    pp.offs = reinterpret_cast<long long*>(ws + pl.ws.offs);
+    pp.cache_stride = a.stride;
+    pp.block_size = a.block_size;
+    pp.block_shift = -1;
+    for (int s = 0; s < 31; ++s)
+        if ((1 << s) == a.block_size) pp.block_shift = s;
+    pp.max_blocks_per_seq = a.max_blocks_per_seq;
     pp.ids = reinterpret_cast<int32_t*>(ws + pl.ws.ids);
     pp.cnt = reinterpret_cast<int32_t*>(ws + pl.ws.cnt);
     pp.qimg = ws + pl.ws.qimg;
@@ -146,8 +157,7 @@ int32_t enqueue(const Args& a, const Plan& pl, uint8_t* ws, cudaEvent_t ev0, cud
     DecodeParams dp{};
     dp.k_cache = static_cast<const uint8_t*>(a.k_cache);
     dp.v_cache = static_cast<const uint8_t*>(a.v_cache);
-    dp.block_tables = a.block_tables;
-    dp.ids = pp.ids;
+    dp.offs = pp.offs;
     dp.cnt = pp.cnt;
     dp.qimg = pp.qimg;
     dp.qscale = pp.qscale;
@@ -155,21 +165,18 @@ int32_t enqueue(const Args& a, const Plan& pl, uint8_t* ws, cudaEvent_t ev0, cud
     dp.part_o = reinterpret_cast<float*>(ws + pl.ws.part_o);
     dp.part_lse = reinterpret_cast<float*>(ws + pl.ws.part_lse);
     dp.status = pp.status;
-    dp.cache_stride = a.stride;
     dp.part = pl.part;
     dp.heads = a.heads;
-    dp.rows_per_seq = a.rows_per_seq;
-    dp.block_size = a.block_size;
-    dp.block_shift = -1;
-    for (int s = 0; s < 31; ++s)
-        if ((1 << s) == a.block_size) dp.block_shift = s;
-    dp.max_blocks_per_seq = a.max_blocks_per_seq;
     dp.kv_same = a.k_cache == a.v_cache ? 1 : 0;
     dp.v_scale = a.v_scale;
-    if (ev0 && cudaEventRecord(ev0, stream) != cudaSuccess) return DSA_ERR_CUDA;
+#ifdef DSA_TRACE
+    dp.trace = g_trace;
+#endif
+    // External records: inside stream capture they become event-record nodes of the graph.
+    if (ev0 && cudaEventRecordWithFlags(ev0, stream, cudaEventRecordExternal) != cudaSuccess) return DSA_ERR_CUDA;
     st = from_cuda(launch_decode(dp, stream));
     if (st != DSA_OK) return st;
-    if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess) return DSA_ERR_CUDA;
+    if (ev1 && cudaEventRecordWithFlags(ev1, stream, cudaEventRecordExternal) != cudaSuccess) return DSA_ERR_CUDA;
 
     if (pl.any_split) {
         CombineParams cp{};
@@ -256,6 +263,10 @@ Args make_args(const void* q, const void* k_cache, const void* v_cache, const in
 }  // namespace
 
 extern "C" {
+
+#ifdef DSA_TRACE
+void dsa_debug_set_trace(void* buffer) { g_trace = static_cast<unsigned long long*>(buffer); }
+#endif
 
 int32_t dsa_abi_version(void) { return 1; }
 

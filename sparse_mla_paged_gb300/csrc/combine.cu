@@ -17,6 +17,8 @@ constexpr int kCombineThreads = 128;  // 4 latent dims per thread
 constexpr int kMaxPieces = 64;        // pieces buffered in shared memory per pass
 
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams p) {
+    // Launched as a programmatic dependent of the decode kernel: wait for its partials.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t u = blockIdx.x;
     const int hl = blockIdx.y;
     const int32_t r = static_cast<int32_t>(u / p.part.groups), g = static_cast<int32_t>(u % p.part.groups);
@@ -83,14 +85,24 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
 
 cudaError_t combine_kernel_setup() {
     cudaFuncAttributes attr;
-    return cudaFuncGetAttributes(&attr, combine_kernel);
+    cudaError_t e = cudaFuncGetAttributes(&attr, combine_kernel);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(combine_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
 }
 
 cudaError_t launch_combine(const CombineParams& p, int units, cudaStream_t stream) {
     if (units <= 0) return cudaSuccess;
-    dim3 grid(units, kHeadsPerCta);
-    combine_kernel<<<grid, kCombineThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(units, kHeadsPerCta);
+    cfg.blockDim = dim3(kCombineThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, combine_kernel, p);
 }
 
 }  // namespace dsa

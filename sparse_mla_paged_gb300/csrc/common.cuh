@@ -32,7 +32,7 @@ constexpr int kStatusTimeout = DSA_ERR_TIMEOUT;
 // Workspace layout (all offsets 256-byte aligned).
 // ------------------------------------------------------------------------------------
 struct WsLayout {
-    size_t status, ids, cnt, qimg, qscale, part_o, part_lse, total;
+    size_t status, ids, offs, cnt, qimg, qscale, part_o, part_lse, total;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -42,6 +42,7 @@ __host__ __device__ inline WsLayout ws_layout(int64_t rows, int64_t groups, int6
     size_t o = 0;
     L.status = o; o += 256;
     L.ids = o; o = align256(o + static_cast<size_t>(rows * width) * 4);
+    L.offs = o; o = align256(o + static_cast<size_t>(rows * width) * 8);
     L.cnt = o; o = align256(o + static_cast<size_t>(rows) * 4);
     L.qimg = o; o = align256(o + static_cast<size_t>(rows * groups) * kQImageBytes);
     L.qscale = o; o = align256(o + static_cast<size_t>(rows * groups) * kHeadsPerCta * 4);
@@ -113,20 +114,23 @@ struct PrologueParams {
     const int32_t* sel;        // [R, W]
     const int32_t* seq_lens;   // [R] or [num_seqs] (verify rows)
     const uint16_t* q;         // bf16 bits [R, H, 512]; null: resolve only
+    const int32_t* block_tables;  // null: ids only, no byte offsets
     int32_t* ids;              // [R, W]
+    long long* offs;           // [R, W] cache byte offset of each resolved token (-1: bad page)
     int32_t* cnt;              // [R]
     uint8_t* qimg;             // [R*G, 64 KB]
     float* qscale;             // [R*G, 64]
     int* status;               // reset by block 0 (may be null)
+    int64_t cache_stride;
     int32_t rows, width, heads, groups, rows_per_seq, verify_rows;
+    int32_t block_size, block_shift, max_blocks_per_seq;
     float score_scale;         // sm_scale * k_scale * log2(e)
 };
 
 struct DecodeParams {
     const uint8_t* k_cache;
     const uint8_t* v_cache;
-    const int32_t* block_tables;
-    const int32_t* ids;
+    const long long* offs;
     const int32_t* cnt;
     const uint8_t* qimg;
     const float* qscale;
@@ -134,11 +138,11 @@ struct DecodeParams {
     float* part_o;             // [2C, 64, 512]
     float* part_lse;           // [2C, 64]
     int* status;
-    int64_t cache_stride;
     Partition part;
-    int32_t heads, rows_per_seq, block_size, block_shift, max_blocks_per_seq;
+    int32_t heads;
     int32_t kv_same;
     float v_scale;
+    unsigned long long* trace;  // per-CTA timeline, used only by -DDSA_TRACE builds
 };
 
 struct CombineParams {
@@ -151,6 +155,9 @@ struct CombineParams {
 };
 
 // Launchers (each defined next to its kernel).
+// The decode and combine kernels are launched as programmatic dependents of the kernel
+// before them on the stream (they start their set-up early and wait on the grid
+// dependency before reading its results).
 cudaError_t launch_prologue(const PrologueParams& p, int blocks, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, int units, cudaStream_t stream);

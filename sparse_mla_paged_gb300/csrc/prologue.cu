@@ -2,7 +2,10 @@
 //
 // Blocks [0, rows) resolve one selection row each (attend.rs module doc: -1 holes,
 // set membership with duplicates collapsed; decode_k.rs: row r only sees positions
-// below its own seq_len): the distinct ids 0 <= id < L in ascending order, -1 padded.
+// below its own seq_len): the distinct ids 0 <= id < L in ascending order, -1 padded,
+// and (for the decode) each id's cache byte offset through the block table
+// (decode_k.rs: physical = block_table[pos / block_size], slot = physical*block_size +
+// pos % block_size), so the decode's gather needs one load per token.
 //   * L <= 262144: a bitmap of L bits in shared memory; ids set with atomicOr and
 //     written out by a block-wide prefix count, which yields them sorted.
 //   * longer rows: bitonic sort of the row in shared memory, then a prefix count of
@@ -51,12 +54,31 @@ __device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t* scra
     return before;
 }
 
+// Byte offset of token `id` of sequence `seq` in the cache, or -1 when the block table
+// has no valid page for it (the decode kernel reports that as a device status).
+__device__ __forceinline__ long long token_offset(const PrologueParams& p, int32_t seq, int32_t id) {
+    const int32_t blk = p.block_shift >= 0 ? (id >> p.block_shift) : id / p.block_size;
+    const int32_t inblk = id - blk * p.block_size;
+    if (p.max_blocks_per_seq > 0 && blk >= p.max_blocks_per_seq) return -1;
+    const int32_t page = p.block_tables[static_cast<int64_t>(seq) * p.max_blocks_per_seq + blk];
+    if (page < 0) return -1;
+    return static_cast<long long>(page) * p.cache_stride + static_cast<long long>(inblk) * kLatent;
+}
+
+__device__ __forceinline__ void emit(const PrologueParams& p, int32_t* ids, long long* offs, int32_t seq,
+                                     int32_t pos, int32_t id) {
+    ids[pos] = id;
+    if (offs) offs[pos] = token_offset(p, seq, id);
+}
+
 __device__ void resolve_row(const PrologueParams& p, int32_t r, uint32_t* sm, int32_t* scratch) {
     const int tid = threadIdx.x;
     const int32_t W = p.width;
     const int32_t L = row_seq_len(p, r);
+    const int32_t seq = r / p.rows_per_seq;
     const int32_t* sel = p.sel + static_cast<int64_t>(r) * W;
     int32_t* ids = p.ids + static_cast<int64_t>(r) * W;
+    long long* offs = p.block_tables ? p.offs + static_cast<int64_t>(r) * W : nullptr;
     int32_t total = 0;
     if (L <= kBitmapWords * 32) {
         const int32_t nwords = (L + 31) >> 5;
@@ -77,7 +99,7 @@ __device__ void resolve_row(const PrologueParams& p, int32_t r, uint32_t* sm, in
             uint32_t bits = sm[w];
             while (bits) {
                 const int b = __ffs(bits) - 1;
-                ids[pos++] = w * 32 + b;
+                emit(p, ids, offs, seq, pos++, w * 32 + b);
                 bits &= bits - 1;
             }
         }
@@ -114,7 +136,7 @@ __device__ void resolve_row(const PrologueParams& p, int32_t r, uint32_t* sm, in
             mine += (keys[j] != INT32_MAX && (j == 0 || keys[j] != keys[j - 1])) ? 1 : 0;
         int32_t pos = block_exclusive_scan(mine, scratch, &total);
         for (int32_t j = j0; j < j1; ++j)
-            if (keys[j] != INT32_MAX && (j == 0 || keys[j] != keys[j - 1])) ids[pos++] = keys[j];
+            if (keys[j] != INT32_MAX && (j == 0 || keys[j] != keys[j - 1])) emit(p, ids, offs, seq, pos++, keys[j]);
     }
     for (int32_t j = total + tid; j < W; j += kResolveThreads) ids[j] = -1;
     if (tid == 0) p.cnt[r] = total;
@@ -185,7 +207,10 @@ __device__ void prepare_queries(const PrologueParams& p, int32_t unit) {
 __global__ void __launch_bounds__(kResolveThreads) prologue_kernel(const PrologueParams p) {
     extern __shared__ __align__(16) uint32_t bitmap[];
     __shared__ int32_t scratch[kResolveThreads / 32];
-    if (blockIdx.x == 0 && threadIdx.x == 0 && p.status) *p.status = 0;
+    // Let the decode kernel launch and run its set-up while this grid finishes; it waits
+    // for this grid's completion before reading anything written here.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (blockIdx.x == 0 && threadIdx.x == 0 && p.status) atomicExch(p.status, 0);
     if (static_cast<int32_t>(blockIdx.x) < p.rows)
         resolve_row(p, blockIdx.x, bitmap, scratch);
     else
@@ -196,7 +221,11 @@ __global__ void __launch_bounds__(kResolveThreads) prologue_kernel(const Prologu
 
 cudaError_t prologue_kernel_setup() {
     cudaFuncAttributes attr;
-    return cudaFuncGetAttributes(&attr, prologue_kernel);
+    cudaError_t e = cudaFuncGetAttributes(&attr, prologue_kernel);
+    if (e != cudaSuccess) return e;
+    // Same shared-memory carveout as the decode kernel, so the SMs need no
+    // reconfiguration between the two.
+    return cudaFuncSetAttribute(prologue_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
 }
 
 cudaError_t launch_prologue(const PrologueParams& p, int blocks, cudaStream_t stream) {

@@ -68,6 +68,32 @@ class Workload:
             self._host = h
         return self._host
 
+    def subset(self, seqs) -> tuple["Workload", list]:
+        """The sequences `seqs` (all their rows) with only their pages, on the CPU.
+
+        The bytes of every page they reference are copied unchanged; pages are renumbered
+        in table order. Returns (workload, row indices of the original)."""
+        seqs = list(seqs)
+        rps = self.rows_per_seq
+        rows = [s * rps + i for s in seqs for i in range(rps)]
+        shared = self.max_blocks_per_seq == 0
+        tables = self.block_tables[[0] if shared else seqs].to(torch.int64)
+        cache = self.k_cache.reshape(self.k_cache.shape[0], -1)
+        pages = tables.reshape(-1)
+        valid = pages >= 0
+        src = torch.where(valid, pages, torch.zeros_like(pages)).to(cache.device)
+        kc = cache[src].cpu()
+        vc = None if self.v_cache is None else self.v_cache.reshape(cache.shape[0], -1)[src].cpu()
+        bt = torch.arange(pages.numel(), dtype=torch.int32).reshape(tables.shape)
+        bt[~valid.cpu().reshape(tables.shape)] = -1
+        sub = Workload(self.name + f" [sequences {seqs}]", self.q[rows].cpu(), kc, vc, bt,
+                       self.seq_lens[rows].cpu(), self.sel_indices[rows].cpu(), len(seqs), rps,
+                       self.num_q_heads, self.block_size, self.cache_stride_bytes,
+                       0 if shared else int(self.block_tables.shape[1]), self.k_scale, self.v_scale,
+                       self.sm_scale, None if self.base_lens is None else self.base_lens[seqs].cpu(),
+                       dict(self.meta))
+        return sub, rows
+
     def to(self, device) -> "Workload":
         def mv(t):
             return None if t is None else t.to(device)
