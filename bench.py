@@ -242,7 +242,7 @@ def run_cuda(args, ws_n, rank, local):
     g = min(K, args.graph_steps)
     reps_per_graph = K // g
     rem = K - reps_per_graph * g
-    n_ev = g + rem
+    n_ev = g
     ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
     ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
     for ev in ev_b + ev_e:                # creates the CUDA events (torch creates them lazily)
@@ -250,25 +250,32 @@ def run_cuda(args, ws_n, rank, local):
     stream.synchronize()
     assert all(ev.cuda_event for ev in ev_b + ev_e)
 
-    def capture(n, base):
+    def capture(n, base, with_events):
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
             with torch.cuda.graph(graph, stream=stream):
                 for j in range(n):
-                    step(base + j, stream, ev_b[base + j], ev_e[base + j])
+                    if with_events:
+                        step(base + j, stream, ev_b[base + j], ev_e[base + j])
+                    else:
+                        step(base + j, stream)
         return graph
 
-    main = capture(g, 0)
-    tail = capture(rem, g) if rem else None
+    # `value` is timed on graphs without event nodes (an event record between two kernels
+    # would cut the programmatic launch overlap); the decode-kernel durations come from a
+    # second graph of the same steps with events around every decode kernel.
+    main = capture(g, 0, False)
+    tail = capture(rem, g, False) if rem else None
+    timing = capture(g, 0, True)
     with torch.cuda.stream(stream):
-        main.replay()                     # untimed replay: warms the graph
+        main.replay()                     # untimed replays: warm the graphs
+        timing.replay()
     stream.synchronize()
 
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    kernel_ms = []
     barrier(ws_n)
     torch.cuda.synchronize()
     wall0 = time.time()
@@ -283,10 +290,10 @@ def run_cuda(args, ws_n, rank, local):
     torch.cuda.synchronize()
     wall1 = time.time()
     barrier(ws_n)
-    # decode-kernel durations: the events hold the last replay of each graph
+    with torch.cuda.stream(stream):
+        timing.replay()
+    stream.synchronize()
     kernel_ms = [event_ms(ev_b[j], ev_e[j]) for j in range(g)]
-    if tail is not None:
-        kernel_ms += [event_ms(ev_b[g + j], ev_e[g + j]) for j in range(rem)]
     clocks = sampler.stop(wall0, wall1)
     total_ms = t_start.elapsed_time(t_end)
     total_ms = max_over_ranks(total_ms, ws_n, device)

@@ -162,7 +162,7 @@ int32_t enqueue(const Args& a, const Plan& pl, uint8_t* ws, cudaEvent_t ev0, cud
     dp.qimg = pp.qimg;
     dp.qscale = pp.qscale;
     dp.out = static_cast<uint16_t*>(a.out);
-    dp.part_o = reinterpret_cast<float*>(ws + pl.ws.part_o);
+    dp.part_o = reinterpret_cast<uint16_t*>(ws + pl.ws.part_o);
     dp.part_lse = reinterpret_cast<float*>(ws + pl.ws.part_lse);
     dp.status = pp.status;
     dp.part = pl.part;

@@ -46,7 +46,7 @@ __host__ __device__ inline WsLayout ws_layout(int64_t rows, int64_t groups, int6
     L.cnt = o; o = align256(o + static_cast<size_t>(rows) * 4);
     L.qimg = o; o = align256(o + static_cast<size_t>(rows * groups) * kQImageBytes);
     L.qscale = o; o = align256(o + static_cast<size_t>(rows * groups) * kHeadsPerCta * 4);
-    L.part_o = o; o = align256(o + static_cast<size_t>(2 * ctas) * kHeadsPerCta * kLatent * 4);
+    L.part_o = o; o = align256(o + static_cast<size_t>(2 * ctas) * kHeadsPerCta * kLatent * 2);
     L.part_lse = o; o = align256(o + static_cast<size_t>(2 * ctas) * kHeadsPerCta * 4);
     L.total = o;
     return L;
@@ -135,7 +135,7 @@ struct DecodeParams {
     const uint8_t* qimg;
     const float* qscale;
     uint16_t* out;             // bf16 bits [R, H, 512]
-    float* part_o;             // [2C, 64, 512]
+    uint16_t* part_o;          // f16 bits [2C, 64, 512]: O / l of a piece, E4M3 code units
     float* part_lse;           // [2C, 64]
     int* status;
     Partition part;
@@ -146,7 +146,7 @@ struct DecodeParams {
 };
 
 struct CombineParams {
-    const float* part_o;
+    const uint16_t* part_o;
     const float* part_lse;
     uint16_t* out;
     Partition part;

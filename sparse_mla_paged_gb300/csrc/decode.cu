@@ -3,20 +3,24 @@
 // One CTA per SM, persistent over a static slot-space partition (see common.cuh). Work
 // unit = (decode row, group of 64 query heads). For each tile of 128 resolved tokens:
 //
-//   gather   warps 0-1   cp.async 16-byte copies of each token's 512-byte E4M3 latent row
-//                        (byte offsets resolved by the prologue; the next tile's offsets
-//                        are prefetched while waiting for a free slot) into a 2-slot ring,
-//                        written in the 128-byte-swizzled K-major operand layout.
-//   QK^T     warp 2      tcgen05.mma kind::f8f6f4, M = 128 tokens, N = 128 (64 heads x
+//   gather   warps 0-3   cp.async 16-byte copies of each token's 512-byte E4M3 latent row
+//                        (byte offsets resolved by the prologue; the next tile's offsets are
+//                        loaded while waiting for a free slot) into a 2-slot ring, written in
+//                        the 128-byte-swizzled K-major operand layout. (Per 512-byte row,
+//                        16-byte copies from 32 lanes sustain a higher gather rate on this
+//                        part than TMA tile::gather4 loads, whose per-instruction cost
+//                        limits an SM to about 17 GB/s.)
+//   QK^T     warp 4      tcgen05.mma kind::f8f6f4, M = 128 tokens, N = 128 (64 heads x
 //                        {hi, lo} query terms), K = 512: S^T -> TMEM (double buffered).
-//   softmax  warps 3-10  two warps per TMEM lane quarter, each thread one token and 32
+//   softmax  warps 5-12  two warps per TMEM lane quarter, each thread one token and 32
 //                        heads: s = hi + lo, per-head scale, column max over the 128 tokens
 //                        (redux.sync.max per warp + a 4-way exchange), online rescale,
 //                        P' = 256*exp2(x - m) stored as two E4M3 terms (hi = top 4 bits,
-//                        lo = rest); the row sums stay per thread until the epilogue.
-//   P.V      warp 2      O^T[512 dims x 64 heads] += V^T * P'^T in TMEM: the same ring slot
+//                        lo = rest); the row sums stay per thread until the epilogue,
+//                        the running maxima in shared memory.
+//   P.V      warp 4      O^T[512 dims x 64 heads] += V^T * P'^T in TMEM: the same ring slot
 //                        read as an MN-major operand (K and V are the same bytes).
-//   epilogue warps 3-10  O / (256 l) * v_scale -> BF16 output, or (O/l, lse) partials,
+//   epilogue warps 5-12  O / (256 l) * v_scale -> BF16 output, or (O/l, lse) partials,
 //                        transposed per warp through shared memory into 16-byte stores.
 //
 // The contraction is exact in its inputs: keys and values are the cached E4M3 codes
@@ -28,6 +32,9 @@
 // S^T buffers at 256 and 384. Every wait is bounded (see ptx.cuh); on a timeout the CTA
 // records DSA_ERR_TIMEOUT, skips the remaining waits and finishes.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <type_traits>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -35,11 +42,11 @@
 namespace dsa {
 namespace {
 
-constexpr int kProducerWarps = 2;
-constexpr int kMmaWarp = 2;
-constexpr int kSoftmaxWarp0 = 3;
+constexpr int kProducerWarps = 4;
+constexpr int kMmaWarp = 4;
+constexpr int kSoftmaxWarp0 = 5;
 constexpr int kSoftmaxWarps = 8;
-constexpr int kThreads = (kSoftmaxWarp0 + kSoftmaxWarps) * 32;  // 352
+constexpr int kThreads = (kSoftmaxWarp0 + kSoftmaxWarps) * 32;  // 416
 constexpr int kProducerThreads = kProducerWarps * 32;
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
 
@@ -54,7 +61,8 @@ constexpr int kOffP = kOffQ + kQImageBytes;              // P' hi (8 KB) then lo
 constexpr int kPTermBytes = kTileTokens * kHeadsPerCta;  // 8 KB
 constexpr int kOffRed = kOffP + 2 * kPTermBytes;         // float [2 parity][4 quarters][64 heads]
 constexpr int kOffCs = kOffRed + 2 * 4 * kHeadsPerCta * 4;
-constexpr int kOffBars = kOffCs + kHeadsPerCta * 4;
+constexpr int kOffM = kOffCs + kHeadsPerCta * 4;         // float [2 parity][64 heads] running max
+constexpr int kOffBars = kOffM + 2 * kHeadsPerCta * 4;
 enum {
     BAR_FULL0, BAR_FULL1, BAR_EMPTY0, BAR_EMPTY1, BAR_SFULL0, BAR_SFULL1, BAR_SEMPTY0, BAR_SEMPTY1,
     BAR_PFULL, BAR_PVDONE, BAR_QFULL, BAR_QEMPTY, BAR_OEMPTY, BAR_DRAIN, BAR_DONE, kNumBars
@@ -171,46 +179,38 @@ __device__ void run_producer(const DecodeParams& p, uint32_t sbase, volatile int
         __syncwarp();
         ++qseg;
         const long long* offs = p.offs + static_cast<int64_t>(s.row) * W + tl.t0;
-        // this lane's two tokens of a tile: warp*64 + lane and warp*64 + 32 + lane
-        const int tok0 = warp * 64 + lane, tok1 = tok0 + 32;
-        long long nx0 = tok0 < tl.n ? offs[tok0] : -1;
-        long long nx1 = tok1 < tl.n ? offs[tok1] : -1;
+        const int tok = warp * 32 + lane;  // this lane's token of each tile
+        long long nx = tok < tl.n ? offs[tok] : -1;
         for (int t = 0; t < tl.ntiles; ++t, ++tau) {
-            const long long o0 = nx0, o1 = nx1;
-            const int32_t base = (t + 1) * kTileTokens;
-            if (t + 1 < tl.ntiles) {  // prefetch the next tile's offsets before waiting
-                nx0 = base + tok0 < tl.n ? offs[base + tok0] : -1;
-                nx1 = base + tok1 < tl.n ? offs[base + tok1] : -1;
-            }
-            const bool in0 = t * kTileTokens + tok0 < tl.n, in1 = t * kTileTokens + tok1 < tl.n;
-            if ((in0 && o0 < 0) || (in1 && o1 < 0)) atomicCAS(p.status, 0, kStatusBounds);
+            const long long o_mine = nx;
+            const int32_t next = (t + 1) * kTileTokens + tok;
+            if (t + 1 < tl.ntiles) nx = next < tl.n ? offs[next] : -1;  // before the slot wait
+            if (t * kTileTokens + tok < tl.n && o_mine < 0) atomicCAS(p.status, 0, kStatusBounds);
             const int slot = static_cast<int>(tau % nslot);
             const uint32_t use = tau / nslot;
             if (tau >= static_cast<uint32_t>(nslot))
                 warp_wait(p, sbase + kOffBars + 8 * (BAR_EMPTY0 + slot), (use - 1) & 1, abort_flag);
+            if (tid == 0 && tau < 8) DSA_TRACE_AT(p, 40 + tau);
             const uint32_t kdst = sbase + kOffRing + slot * kKvTileBytes;
             const uint32_t vdst = p.kv_same ? kdst : sbase + kOffRing + kKvTileBytes;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const long long mine = half ? o1 : o0;
 #pragma unroll 4
-                for (int j = 0; j < 32; ++j) {
-                    const long long o = __shfl_sync(0xffffffffu, mine, j);
-                    const int tk = warp * 64 + half * 32 + j;
-                    const uint32_t d = chunk + tk * 128 + (((lane & 7) ^ (tk & 7)) << 4);
-                    if (o >= 0) {
-                        cp_async_16(kdst + d, p.k_cache + o + lane * 16);
-                        if (!p.kv_same) cp_async_16(vdst + d, p.v_cache + o + lane * 16);
-                    } else {
-                        st_shared_v4(kdst + d, 0u, 0u, 0u, 0u);
-                        if (!p.kv_same) st_shared_v4(vdst + d, 0u, 0u, 0u, 0u);
-                    }
+            for (int j = 0; j < 32; ++j) {
+                const long long o = __shfl_sync(0xffffffffu, o_mine, j);
+                const int tk = warp * 32 + j;
+                const uint32_t d = chunk + tk * 128 + (((lane & 7) ^ (tk & 7)) << 4);
+                if (o >= 0) {
+                    cp_async_16(kdst + d, p.k_cache + o + lane * 16);
+                    if (!p.kv_same) cp_async_16(vdst + d, p.v_cache + o + lane * 16);
+                } else {
+                    st_shared_v4(kdst + d, 0u, 0u, 0u, 0u);
+                    if (!p.kv_same) st_shared_v4(vdst + d, 0u, 0u, 0u, 0u);
                 }
             }
             const uint32_t fb = sbase + kOffBars + 8 * (BAR_FULL0 + slot);
             cp_async_arrive_noinc(fb);
             mbar_arrive(fb);
             if (tid == 0 && tau == 0) DSA_TRACE_AT(p, 4);
+            if (tid == 0 && tau < 8) DSA_TRACE_AT(p, 48 + tau);
         }
     }
     if (tid == 0) DSA_TRACE_AT(p, 5);
@@ -251,35 +251,60 @@ __device__ void run_mma(const DecodeParams& p, uint32_t sbase, uint32_t tmem, vo
         tc_commit(barp(BAR_EMPTY0 + slot));
     };
 
+    auto issue_qk = [&](uint32_t tq) {
+        const int slot = static_cast<int>(tq % nslot);
+        const int sb = tq & 1;
+        fence_proxy_async_smem();
+        tc_fence_after();
+        const uint32_t kbase = sbase + kOffRing + slot * kKvTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < 16; ++ks) {
+            const uint32_t off = (ks >> 2) * kKBlockBytes + (ks & 3) * 32;
+            mma_e4m3(tmem + kTmemS + sb * 128, smem_desc(kbase + off, 16, 1024, kSwizzle128B),
+                     smem_desc(sbase + kOffQ + off, 16, 1024, kSwizzle128B), idq, ks > 0 ? 1u : 0u);
+        }
+        tc_commit(barp(BAR_SFULL0 + sb));
+        if (tq == 0) DSA_TRACE_AT(p, 8);
+    };
+    // Phase the QK of tile tq may start: its ring slot is full and its S buffer is free.
+    auto qk_ready = [&](uint32_t tq) {
+        const int slot = static_cast<int>(tq % nslot);
+        const bool full = mbar_try_wait(barp(BAR_FULL0 + slot), (tq / nslot) & 1);
+        return full && (tq < 2 || mbar_try_wait(barp(BAR_SEMPTY0 + (tq & 1)), ((tq >> 1) - 1) & 1));
+    };
+
     for (int i = 0; i < nseg; ++i) {
         const Segment s = cta_segment(p.part, blockIdx.x, i);
         const Tiles tl = segment_tokens(p, s);
         if (tl.n <= 0) continue;
         if (!mbar_wait(barp(BAR_QFULL), qseg & 1, abort_flag)) fail(p, abort_flag, kStatusTimeout);
         if (qseg == 0) DSA_TRACE_AT(p, 6);
+        const uint32_t tau0 = tau;
+        // QK(t) and PV(t-1) are independent: issue whichever becomes ready first (with one
+        // ring slot, QK(t) needs the slot PV(t-1) frees, so PV(t-1) goes first).
         for (int t = 0; t < tl.ntiles; ++t, ++tau) {
-            if (nslot == 1 && t > 0) issue_pv(tau - 1, t == 1);
-            const int slot = static_cast<int>(tau % nslot);
-            const uint32_t use = tau / nslot;
-            if (!mbar_wait(barp(BAR_FULL0 + slot), use & 1, abort_flag)) fail(p, abort_flag, kStatusTimeout);
-            if (tau == 0) DSA_TRACE_AT(p, 7);
-            if (tau < 8) DSA_TRACE_AT(p, 56 + tau);
-            const int sb = tau & 1;
-            if (tau >= 2 && !mbar_wait(barp(BAR_SEMPTY0 + sb), ((tau >> 1) - 1) & 1, abort_flag))
-                fail(p, abort_flag, kStatusTimeout);
-            fence_proxy_async_smem();
-            tc_fence_after();
-            const uint32_t kbase = sbase + kOffRing + slot * kKvTileBytes;
-#pragma unroll
-            for (int ks = 0; ks < 16; ++ks) {
-                const uint32_t off = (ks >> 2) * kKBlockBytes + (ks & 3) * 32;
-                mma_e4m3(tmem + kTmemS + sb * 128, smem_desc(kbase + off, 16, 1024, kSwizzle128B),
-                         smem_desc(sbase + kOffQ + off, 16, 1024, kSwizzle128B), idq, ks > 0 ? 1u : 0u);
+            bool qk_done = false, pv_done = (t == 0);
+            if (nslot == 1 && !pv_done) {
+                issue_pv(tau - 1, tau - 1 == tau0);
+                pv_done = true;
             }
-            tc_commit(barp(BAR_SFULL0 + sb));
-            if (tau == 0) DSA_TRACE_AT(p, 8);
-            if (t == tl.ntiles - 1) tc_commit(barp(BAR_QEMPTY));
-            if (nslot == 2 && t > 0) issue_pv(tau - 1, t == 1);
+            const uint64_t t_start = globaltimer_ns();
+            while (!qk_done || !pv_done) {
+                if (!qk_done && qk_ready(tau)) {
+                    if (tau < 8) DSA_TRACE_AT(p, 56 + tau);
+                    issue_qk(tau);
+                    if (t == tl.ntiles - 1) tc_commit(barp(BAR_QEMPTY));
+                    qk_done = true;
+                }
+                if (!pv_done && mbar_try_wait(barp(BAR_PFULL), (tau - 1) & 1)) {
+                    issue_pv(tau - 1, tau - 1 == tau0);
+                    pv_done = true;
+                }
+                if ((!qk_done || !pv_done) && (*abort_flag || globaltimer_ns() - t_start > kWaitLimitNs)) {
+                    fail(p, abort_flag, kStatusTimeout);
+                    break;
+                }
+            }
         }
         issue_pv(tau - 1, tl.ntiles == 1);
         ++qseg;
@@ -293,7 +318,7 @@ __device__ void run_mma(const DecodeParams& p, uint32_t sbase, uint32_t tmem, vo
 
 // Writes a warp's 32 dims x 16 heads block (dims on lanes, v[k] = head h0+k, scaled by
 // f[k]) to row-major global rows (row stride kLatent elements) through a 2 KB per-warp
-// staging area, with 16-byte stores. T is float (partials) or bf16 (output). Heads at or
+// staging area, with 16-byte stores. T is bf16 (output) or f16 (partials). Heads at or
 // beyond hvalid are not written.
 template <typename T>
 __device__ __forceinline__ void store_block(T* rows, int h0, int hvalid, int dim0, const float* v, const float* f,
@@ -305,8 +330,8 @@ __device__ __forceinline__ void store_block(T* rows, int h0, int hvalid, int dim
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
         const float x = v[k] * f[k];
-        if constexpr (sizeof(T) == 4) {
-            stg[k * 32 + lane] = x;
+        if constexpr (std::is_same<T, __half>::value) {
+            stg[k * 32 + lane] = __float2half_rn(x);
         } else {
             stg[k * 32 + lane] = __float2bfloat16_rn(x);
         }
@@ -334,6 +359,7 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
     const int st = sw * 32 + lane;            // 0..255
     float* red = reinterpret_cast<float*>(smem + kOffRed);   // [2][4][64]
     float* c_s = reinterpret_cast<float*>(smem + kOffCs);
+    float* m_s = reinterpret_cast<float*>(smem + kOffM);     // [2][64]
     uint8_t* stage = smem + kOffP + sw * 2048;               // epilogue staging (2 KB per warp)
     auto barp = [&](int b) { return sbase + kOffBars + 8 * b; };
     const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
@@ -350,8 +376,8 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
                 uint4* o = reinterpret_cast<uint4*>(p.out + head0 * kLatent);
                 for (int e = st; e < hvalid * kLatent / 8; e += kSoftmaxThreads) o[e] = make_uint4(0, 0, 0, 0);
             } else {
-                float4* po = reinterpret_cast<float4*>(p.part_o + static_cast<int64_t>(s.part) * kHeadsPerCta * kLatent);
-                for (int e = st; e < kHeadsPerCta * kLatent / 4; e += kSoftmaxThreads) po[e] = make_float4(0, 0, 0, 0);
+                uint4* po = reinterpret_cast<uint4*>(p.part_o + static_cast<int64_t>(s.part) * kHeadsPerCta * kLatent);
+                for (int e = st; e < kHeadsPerCta * kLatent / 8; e += kSoftmaxThreads) po[e] = make_uint4(0, 0, 0, 0);
                 if (st < kHeadsPerCta) p.part_lse[s.part * kHeadsPerCta + st] = kNegInf;
             }
             continue;
@@ -360,17 +386,14 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
         named_bar_sync<kBarSoftmax, kSoftmaxThreads>();
         if (st == 0 && i == 0) DSA_TRACE_AT(p, 12);
 
-        float m_run[32], l_part[32];
+        float l_part[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-            m_run[k] = kNegInf;
-            l_part[k] = 0.0f;
-        }
+        for (int k = 0; k < 32; ++k) l_part[k] = 0.0f;
         for (int t = 0; t < tl.ntiles; ++t, ++tau) {
             const int sb = tau & 1;
             warp_wait(p, barp(BAR_SFULL0 + sb), (tau >> 1) & 1, abort_flag);
             if (st == 0 && tau == 0) DSA_TRACE_AT(p, 13);
-            if (st == 0 && tau < 16) DSA_TRACE_AT(p, 24 + tau);
+            if (st == 0 && tau < 8) DSA_TRACE_AT(p, 24 + tau);
             tc_fence_after();
             float x[32];
             {
@@ -379,9 +402,13 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
                 tmem_ld_x32(ta, a);        // hi-term scores of heads h0..h0+31
 #pragma unroll
                 for (int k = 0; k < 32; ++k) x[k] = __uint_as_float(a[k]);
-                tmem_ld_x32(ta + 64, a);   // lo-term scores
 #pragma unroll
-                for (int k = 0; k < 32; ++k) x[k] += __uint_as_float(a[k]);
+                for (int half = 0; half < 2; ++half) {  // lo-term scores, 16 columns at a time
+                    uint32_t b[16];
+                    tmem_ld_x16(ta + 64 + half * 16, b);
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) x[half * 16 + k] += __uint_as_float(b[k]);
+                }
             }
             tc_fence_before();
             __syncwarp();
@@ -409,30 +436,26 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
             }
             half_bar_sync(hh);
             if (st == 0 && tau == 0) DSA_TRACE_AT(p, 14);
-            uint32_t grew = 0;
-            float al[32];
+            // Lane k owns head h0+k: tile max over the 4 quarters, running max (parity (t-1)&1
+            // in m_s, -inf before the first tile), new max and rescale factor alpha. The new max
+            // goes to parity t&1 (all four warps of the half write the same values), read back
+            // only after the next half barrier. Every lane then takes head k's values by
+            // shuffle as it uses them.
+            const int hk = h0 + lane;
+            const float mt = fmaxf(fmaxf(rbuf[hk], rbuf[kHeadsPerCta + hk]),
+                                   fmaxf(rbuf[2 * kHeadsPerCta + hk], rbuf[3 * kHeadsPerCta + hk]));
+            const float mo = t > 0 ? m_s[((t + 1) & 1) * kHeadsPerCta + hk] : kNegInf;
+            const float mn = fmaxf(mo, mt);
+            const float a_mine = (mo == kNegInf) ? 0.0f : ex2_approx(mo - mn);
+            m_s[(t & 1) * kHeadsPerCta + hk] = mn;
+            const uint32_t grew = __ballot_sync(0xffffffffu, a_mine < 1.0f);
 #pragma unroll
-            for (int k = 0; k < 32; k += 4) {
-                const float4 r0 = *reinterpret_cast<const float4*>(rbuf + 0 * kHeadsPerCta + h0 + k);
-                const float4 r1 = *reinterpret_cast<const float4*>(rbuf + 1 * kHeadsPerCta + h0 + k);
-                const float4 r2 = *reinterpret_cast<const float4*>(rbuf + 2 * kHeadsPerCta + h0 + k);
-                const float4 r3 = *reinterpret_cast<const float4*>(rbuf + 3 * kHeadsPerCta + h0 + k);
-                const float mt[4] = {fmaxf(fmaxf(r0.x, r1.x), fmaxf(r2.x, r3.x)),
-                                     fmaxf(fmaxf(r0.y, r1.y), fmaxf(r2.y, r3.y)),
-                                     fmaxf(fmaxf(r0.z, r1.z), fmaxf(r2.z, r3.z)),
-                                     fmaxf(fmaxf(r0.w, r1.w), fmaxf(r2.w, r3.w))};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float mo = m_run[k + e];
-                    const float mn = fmaxf(mo, mt[e]);
-                    const float a = (mo == kNegInf) ? 0.0f : ex2_approx(mo - mn);
-                    grew |= (a < 1.0f ? 1u : 0u) << (k + e);
-                    al[k + e] = a;
-                    m_run[k + e] = mn;
-                    const float pr = ex2_approx(x[k + e] - mn);
-                    l_part[k + e] = l_part[k + e] * a + pr;
-                    x[k + e] = pr;
-                }
+            for (int k = 0; k < 32; ++k) {
+                const float m_k = __shfl_sync(0xffffffffu, mn, k);
+                const float a_k = __shfl_sync(0xffffffffu, a_mine, k);
+                const float pr = ex2_approx(x[k] - m_k);
+                l_part[k] = l_part[k] * a_k + pr;
+                x[k] = pr;
             }
             // P and O may only change once the previous P.V has finished reading them.
             if (t > 0) warp_wait(p, barp(BAR_PVDONE), (tau - 1) & 1, abort_flag);
@@ -457,6 +480,9 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
             }
             if (t > 0 && grew != 0u) {
                 // Rescale this half's O^T columns by alpha (1 for heads whose max held).
+                float al[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k) al[k] = __shfl_sync(0xffffffffu, a_mine, k);
                 tc_fence_after();
 #pragma unroll 1
                 for (int mc = 0; mc < 4; ++mc) {
@@ -474,54 +500,44 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
             __syncwarp();
             if (lane == 0) mbar_arrive(barp(BAR_PFULL));
             if (st == 0 && tau == 0) DSA_TRACE_AT(p, 16);
-            if (st == 0 && tau < 16) DSA_TRACE_AT(p, 40 + tau);
+            if (st == 0 && tau < 8) DSA_TRACE_AT(p, 32 + tau);
         }
 
         // ---- epilogue ----
         warp_wait(p, barp(BAR_PVDONE), (tau - 1) & 1, abort_flag);
         if (st == 0 && i == 0) DSA_TRACE_AT(p, 17);
         tc_fence_after();
-        // Row sums: this thread's token over its 32 heads -> per head over the warp (lane k
-        // ends with head h0+k) -> over the 4 quarters.
-        {
-            float v[32];
+        // Row sums: per head over the warp's 32 tokens (butterfly, result in every lane),
+        // then over the 4 lane quarters through shared memory.
 #pragma unroll
-            for (int k = 0; k < 32; ++k) v[k] = l_part[k];
-#define DSA_SUM_STEP(W, OFF)                                                    \
-    {                                                                           \
-        const bool upper = (lane & (OFF)) != 0;                                 \
-        _Pragma("unroll") for (int k = 0; k < (W); ++k) {                       \
-            const float send = upper ? v[k] : v[k + (W)];                       \
-            const float keep = upper ? v[k + (W)] : v[k];                       \
-            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, (OFF));            \
-        }                                                                       \
-    }
-            DSA_SUM_STEP(16, 16)
-            DSA_SUM_STEP(8, 8)
-            DSA_SUM_STEP(4, 4)
-            DSA_SUM_STEP(2, 2)
-            DSA_SUM_STEP(1, 1)
-#undef DSA_SUM_STEP
-            red[q4 * kHeadsPerCta + h0 + lane] = v[0];   // parity-0 half of the scratch
+        for (int k = 0; k < 32; ++k) {
+            float v = l_part[k];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+            l_part[k] = v;
+        }
+        if (st == 0 && i == 0) DSA_TRACE_AT(p, 2);
+        if (lane == 0) {
+#pragma unroll
+            for (int k = 0; k < 32; k += 4)
+                *reinterpret_cast<float4*>(red + q4 * kHeadsPerCta + h0 + k) =
+                    make_float4(l_part[k], l_part[k + 1], l_part[k + 2], l_part[k + 3]);
         }
         half_bar_sync(hh);
-        float f[32];
+        // Lane k: head h0+k's row sum, output factor and (for a partial) log-sum-exp.
         const bool whole = s.part < 0;
-#pragma unroll
-        for (int k = 0; k < 32; k += 4) {
-            const float4 r0 = *reinterpret_cast<const float4*>(red + 0 * kHeadsPerCta + h0 + k);
-            const float4 r1 = *reinterpret_cast<const float4*>(red + 1 * kHeadsPerCta + h0 + k);
-            const float4 r2 = *reinterpret_cast<const float4*>(red + 2 * kHeadsPerCta + h0 + k);
-            const float4 r3 = *reinterpret_cast<const float4*>(red + 3 * kHeadsPerCta + h0 + k);
-            const float l[4] = {(r0.x + r1.x) + (r2.x + r3.x), (r0.y + r1.y) + (r2.y + r3.y),
-                                (r0.z + r1.z) + (r2.z + r3.z), (r0.w + r1.w) + (r2.w + r3.w)};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                f[k + e] = (whole ? p.v_scale : 1.0f) / (kPScale * l[e]);
-                if (!whole && q4 == 0 && lane == 0)
-                    p.part_lse[s.part * kHeadsPerCta + h0 + k + e] = m_run[k + e] + __log2f(l[e]);
-            }
+        float f_mine;
+        {
+            const int hk = h0 + lane;
+            const float l = (red[hk] + red[kHeadsPerCta + hk]) + (red[2 * kHeadsPerCta + hk] + red[3 * kHeadsPerCta + hk]);
+            f_mine = (whole ? p.v_scale : 1.0f) / (kPScale * l);
+            if (!whole && q4 == 0)
+                p.part_lse[s.part * kHeadsPerCta + hk] = m_s[((tl.ntiles - 1) & 1) * kHeadsPerCta + hk] + __log2f(l);
         }
+        float f[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) f[k] = __shfl_sync(0xffffffffu, f_mine, k);
+        if (st == 0 && i == 0) DSA_TRACE_AT(p, 15);
 #pragma unroll 1
         for (int mc = 0; mc < 4; ++mc) {
             uint32_t v[32];
@@ -535,10 +551,11 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
                 store_block(rows, h0, hvalid, dim0, o, f, stage, lane);
                 store_block(rows, h0 + 16, hvalid, dim0, o + 16, f + 16, stage, lane);
             } else {
-                float* rows = p.part_o + static_cast<int64_t>(s.part) * kHeadsPerCta * kLatent;
+                __half* rows = reinterpret_cast<__half*>(p.part_o) + static_cast<int64_t>(s.part) * kHeadsPerCta * kLatent;
                 store_block(rows, h0, kHeadsPerCta, dim0, o, f, stage, lane);
                 store_block(rows, h0 + 16, kHeadsPerCta, dim0, o + 16, f + 16, stage, lane);
             }
+            if (st == 0 && i == 0 && mc == 0) DSA_TRACE_AT(p, 23);
         }
         tc_fence_before();
         __syncwarp();
@@ -561,6 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
 
     if (tid == 0) {
         const uint32_t b = sbase + kOffBars;
+        // one cp.async arrival and one plain arrival per gather thread
         mbar_init(b + 8 * BAR_FULL0, 2 * kProducerThreads);
         mbar_init(b + 8 * BAR_FULL1, 2 * kProducerThreads);
         mbar_init(b + 8 * BAR_EMPTY0, 1);

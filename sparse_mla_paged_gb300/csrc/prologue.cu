@@ -65,11 +65,6 @@ __device__ __forceinline__ long long token_offset(const PrologueParams& p, int32
     return static_cast<long long>(page) * p.cache_stride + static_cast<long long>(inblk) * kLatent;
 }
 
-__device__ __forceinline__ void emit(const PrologueParams& p, int32_t* ids, long long* offs, int32_t seq,
-                                     int32_t pos, int32_t id) {
-    ids[pos] = id;
-    if (offs) offs[pos] = token_offset(p, seq, id);
-}
 
 __device__ void resolve_row(const PrologueParams& p, int32_t r, uint32_t* sm, int32_t* scratch) {
     const int tid = threadIdx.x;
@@ -99,7 +94,7 @@ __device__ void resolve_row(const PrologueParams& p, int32_t r, uint32_t* sm, in
             uint32_t bits = sm[w];
             while (bits) {
                 const int b = __ffs(bits) - 1;
-                emit(p, ids, offs, seq, pos++, w * 32 + b);
+                ids[pos++] = w * 32 + b;
                 bits &= bits - 1;
             }
         }
@@ -136,10 +131,29 @@ __device__ void resolve_row(const PrologueParams& p, int32_t r, uint32_t* sm, in
             mine += (keys[j] != INT32_MAX && (j == 0 || keys[j] != keys[j - 1])) ? 1 : 0;
         int32_t pos = block_exclusive_scan(mine, scratch, &total);
         for (int32_t j = j0; j < j1; ++j)
-            if (keys[j] != INT32_MAX && (j == 0 || keys[j] != keys[j - 1])) emit(p, ids, offs, seq, pos++, keys[j]);
+            if (keys[j] != INT32_MAX && (j == 0 || keys[j] != keys[j - 1])) ids[pos++] = keys[j];
     }
     for (int32_t j = total + tid; j < W; j += kResolveThreads) ids[j] = -1;
     if (tid == 0) p.cnt[r] = total;
+    if (!offs) return;
+    // Byte offsets, four independent id and block-table loads in flight per thread.
+    __syncthreads();
+    for (int32_t j0 = tid; j0 < total; j0 += 4 * kResolveThreads) {
+        int32_t id[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int32_t j = j0 + e * kResolveThreads;
+            id[e] = j < total ? ids[j] : 0;
+        }
+        long long o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[e] = token_offset(p, seq, id[e]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int32_t j = j0 + e * kResolveThreads;
+            if (j < total) offs[j] = o[e];
+        }
+    }
 }
 
 // One (row, group): 8 warps x 8 heads; lane l handles latent dims [16l, 16l+16).
@@ -147,26 +161,35 @@ __device__ void prepare_queries(const PrologueParams& p, int32_t unit) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int32_t r = unit / p.groups, g = unit % p.groups;
     uint8_t* img = p.qimg + static_cast<int64_t>(unit) * kQImageBytes;
-    for (int hl = warp; hl < kHeadsPerCta; hl += kResolveThreads / 32) {
-        const int32_t h = g * kHeadsPerCta + hl;
-        float x[16];
+    constexpr int kHeadsPerWarp = kHeadsPerCta / (kResolveThreads / 32);  // 8
+    // All of this warp's loads first (8 heads x 32 bytes per lane), then the arithmetic.
+    uint4 raw[kHeadsPerWarp][2];
+#pragma unroll
+    for (int i = 0; i < kHeadsPerWarp; ++i) {
+        const int32_t h = g * kHeadsPerCta + warp + i * (kResolveThreads / 32);
         if (h < p.heads) {
             const uint4* src = reinterpret_cast<const uint4*>(
                 p.q + (static_cast<int64_t>(r) * p.heads + h) * kLatent + lane * 16);
-            const uint4 a = src[0], b = src[1];
-            const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                x[2 * i] = __uint_as_float(w[i] << 16);
-                x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-            }
+            raw[i][0] = src[0];
+            raw[i][1] = src[1];
         } else {
+            raw[i][0] = raw[i][1] = make_uint4(0, 0, 0, 0);
+        }
+    }
 #pragma unroll
-            for (int i = 0; i < 16; ++i) x[i] = 0.0f;
+    for (int i = 0; i < kHeadsPerWarp; ++i) {
+        const int hl = warp + i * (kResolveThreads / 32);
+        float x[16];
+        const uint32_t w[8] = {raw[i][0].x, raw[i][0].y, raw[i][0].z, raw[i][0].w,
+                               raw[i][1].x, raw[i][1].y, raw[i][1].z, raw[i][1].w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            x[2 * k] = __uint_as_float(w[k] << 16);
+            x[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
         }
         float amax = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+        for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(x[k]));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         // e with amax * 2^e in [128, 256): amax = 1.m * 2^(E-127), so e = 134 - E.
@@ -176,19 +199,19 @@ __device__ void prepare_queries(const PrologueParams& p, int32_t unit) {
             e = 134 - E;
             e = e > 126 ? 126 : (e < -126 ? -126 : e);
         }
-        const float s = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+        const float sc = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
         uint32_t hi[4], lo[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float v[4], vh[4], vl[4];
+        for (int k = 0; k < 4; ++k) {
+            float vh[4], vl[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                v[k] = x[4 * i + k] * s;
-                vh[k] = __uint_as_float(__float_as_uint(v[k]) & 0xFFF00000u);
-                vl[k] = v[k] - vh[k];
+            for (int m = 0; m < 4; ++m) {
+                const float v = x[4 * k + m] * sc;
+                vh[m] = __uint_as_float(__float_as_uint(v) & 0xFFF00000u);
+                vl[m] = v - vh[m];
             }
-            hi[i] = f32x2_to_e4m3x2(vh[0], vh[1]) | (f32x2_to_e4m3x2(vh[2], vh[3]) << 16);
-            lo[i] = f32x2_to_e4m3x2(vl[0], vl[1]) | (f32x2_to_e4m3x2(vl[2], vl[3]) << 16);
+            hi[k] = f32x2_to_e4m3x2(vh[0], vh[1]) | (f32x2_to_e4m3x2(vh[2], vh[3]) << 16);
+            lo[k] = f32x2_to_e4m3x2(vl[0], vl[1]) | (f32x2_to_e4m3x2(vl[2], vl[3]) << 16);
         }
         // K-major SW128 image: K-block kb = lane/8 (128 dims), 16-byte chunk c = lane%8,
         // row j stored at kb*16K + j*128 with its chunks permuted by j%8.
