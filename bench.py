@@ -36,6 +36,10 @@ L2_BYTES = 129 * 1024 * 1024
 WORKLOADS = {"tiny": 0, "decode_batch": 1, "ragged": 2, "pooled_128k": 3, "verify_k4": 4}
 DEFAULT_WORKLOAD = "decode_batch"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# DRAM bytes (read + write) of one decode-kernel launch, from the ncu capture of the
+# current kernel summarised under profiles/ (decode_kernel_<workload>.md). A workload
+# absent here reports traffic null; an entry is removed whenever the kernel changes.
+MEASURED_TRAFFIC = {"decode_batch": 8961280 + 0}
 
 
 # ----------------------------------------------------------------------------------------
@@ -318,7 +322,8 @@ def run_cuda(args, ws_n, rank, local):
         achieved = cost["flops"] / (kernel_us * 1e-6) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": tf, "unit": "TFLOP/s",
                 "frac": round(achieved / tf, 4)}
-    roof.update({"traffic": args.traffic, "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if
+    traffic = args.traffic if args.traffic is not None else MEASURED_TRAFFIC.get(args.workload)
+    roof.update({"traffic": traffic, "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if
                  peak_src == "measured" else "fallback (6.8 TB/s, 1.9 PFLOP/s)",
                  "kernel": "decode_kernel", "kernel_us": round(kernel_us, 3),
                  "step_roofline_us": round(roof_us, 3), "step_frac": round(roof_us / us_per_step, 4)})
