@@ -180,6 +180,30 @@ int32_t dsa_resolve_indices(const int32_t* sel_indices, const int32_t* seq_lens,
                             int32_t* counts_out, void* stream);
 
 /*
+ * dsa_mla_decode_static: dsa_mla_decode for callers that cannot allocate device memory at
+ * call time (for instance code running under a framework that owns all device memory
+ * through its own pool, or a latency-critical path that cannot accept cudaMalloc's
+ * device-wide synchronisation) and that do not keep a workspace of their own. Arguments,
+ * semantics and errors as dsa_mla_decode; it never calls cudaMalloc, cudaFree or any
+ * allocating routine. Its scratch is a fixed device array of DSA_STATIC_SCRATCH_BYTES
+ * (40 MiB) in the library, present on every GPU that loads the library until the process
+ * exits; a shape whose workspace (dsa_mla_decode_workspace_bytes with num_ctas = 0) is
+ * larger returns DSA_ERR_WORKSPACE and enqueues nothing.
+ *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ *    with that device current; make that first call before any stream capture.
+ *  - All calls share the one array: calls whose work overlaps on the GPU (other streams or
+ *    threads) race on it and must be serialised by the caller.
+ * The source pages have no counterpart to this entry point.
+ */
+#define DSA_STATIC_SCRATCH_BYTES (40u * 1024u * 1024u)
+int32_t dsa_mla_decode_static(const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_tables, int32_t max_blocks_per_seq,
+                              const int32_t* seq_lens, const int32_t* sel_indices, int32_t sel_width,
+                              int32_t num_seqs, int32_t rows_per_seq, int32_t num_q_heads,
+                              int32_t block_size, int64_t cache_stride_bytes, float k_scale,
+                              float v_scale, float sm_scale, void* out, void* stream);
+
+/*
  * Device status of the latest call on a caller workspace (dsa_mla_decode_ws /
  * dsa_mla_decode_host) or on the library workspace of the current device
  * (dsa_last_device_status). Synchronises the stream, writes the status to *status_out

@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdsa_mla.so")
-SOURCES = ["api.cu", "prologue.cu", "decode.cu", "combine.cu"]
+SOURCES = ["api.cu", "prologue.cu", "decode.cu", "combine.cu", "static_scratch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
