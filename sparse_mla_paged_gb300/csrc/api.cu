@@ -113,7 +113,7 @@ Plan make_plan(int64_t rows, int32_t heads, int32_t width, int32_t num_ctas, int
     pl.part.groups = static_cast<int32_t>(pl.groups);
     int64_t c = num_ctas;
     if (c <= 0) {
-        c = (pl.part.total_slots + kTileTokens - 1) / kTileTokens;
+        c = (pl.part.total_slots + kCtaMinSlots - 1) / kCtaMinSlots;
         if (c > sms) c = sms;
         if (c < 1) c = 1;
     }
@@ -172,11 +172,18 @@ int32_t enqueue(const Args& a, const Plan& pl, uint8_t* ws, cudaEvent_t ev0, cud
 #ifdef DSA_TRACE
     dp.trace = g_trace;
 #endif
-    // External records: inside stream capture they become event-record nodes of the graph.
-    if (ev0 && cudaEventRecordWithFlags(ev0, stream, cudaEventRecordExternal) != cudaSuccess) return DSA_ERR_CUDA;
+    // Inside stream capture the records must be external, so that they become event-record
+    // nodes of the graph; outside capture they are plain records.
+    unsigned int ev_flags = cudaEventRecordDefault;
+    if (ev0 || ev1) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return DSA_ERR_CUDA;
+        if (cs == cudaStreamCaptureStatusActive) ev_flags = cudaEventRecordExternal;
+    }
+    if (ev0 && cudaEventRecordWithFlags(ev0, stream, ev_flags) != cudaSuccess) return DSA_ERR_CUDA;
     st = from_cuda(launch_decode(dp, stream));
     if (st != DSA_OK) return st;
-    if (ev1 && cudaEventRecordWithFlags(ev1, stream, cudaEventRecordExternal) != cudaSuccess) return DSA_ERR_CUDA;
+    if (ev1 && cudaEventRecordWithFlags(ev1, stream, ev_flags) != cudaSuccess) return DSA_ERR_CUDA;
 
     if (pl.any_split) {
         CombineParams cp{};

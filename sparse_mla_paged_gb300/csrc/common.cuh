@@ -12,17 +12,23 @@
 namespace dsa {
 
 constexpr int kLatent = 512;           // kv_lora_rank: the whole cache token (NoPE)
-constexpr int kTileTokens = 128;       // tokens per tile = MMA M of the score product
+constexpr int kTileTokens = 128;       // tokens per decode tile = MMA N of the score product
+constexpr int kCtaMinSlots = 128;      // default grid: at least this many slots per CTA
 constexpr int kHeadsPerCta = 64;       // query heads per work unit
-constexpr int kQImageBytes = 2 * kHeadsPerCta * kLatent;  // E4M3 hi + lo terms, 64 KB
+// Query operand image of one unit: 128 rows of 512 E4M3 codes, row 32*q + 2*k + t holding
+// term t (0 = hi, 1 = lo) of head 16*q + k, dims in natural order.
+constexpr int kQImageBytes = 2 * kHeadsPerCta * kLatent;  // 64 KB
 constexpr int kKvTileBytes = kTileTokens * kLatent;       // 64 KB of E4M3 per tile
-constexpr int kKBlockBytes = kTileTokens * 128;           // one 128-dim slab of a tile
 constexpr int kBitmapWords = 8192;     // resolve bitmap: seq_len up to 262144 tokens
 constexpr int kResolveThreads = 256;
 
-// Score-probability scaling: P' = 256 * exp2(x - m) lies in [0, 256] and is carried as
-// two E4M3 terms (see decode.cu).
-constexpr float kPScale = 256.0f;
+// Probabilities are carried as P' = 2^(x - m + kPBias) (x, m in log2 units) split into two
+// E4M3 terms. A head's reference max m is raised, to its tile max plus kRescaleSlack, only
+// when a tile's score exceeds m by more than kRescaleMargin; so P' stays below
+// 2^(kPBias + kRescaleMargin) < 448, the E4M3 maximum, and rescales are rare.
+constexpr float kPBias = 7.0f;
+constexpr float kRescaleMargin = 1.75f;
+constexpr float kRescaleSlack = 2.0f;
 
 // Device status codes mirror dsa_status.
 constexpr int kStatusBounds = DSA_ERR_DEVICE_BOUNDS;

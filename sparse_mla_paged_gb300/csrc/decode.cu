@@ -1,36 +1,35 @@
 // The selected-index NoPE MLA paged decode kernel (attend.rs, decode_attention).
 //
 // One CTA per SM, persistent over a static slot-space partition (see common.cuh). Work
-// unit = (decode row, group of 64 query heads). For each tile of 128 resolved tokens:
+// unit = (decode row, group of 64 query heads). Tiles of 128 resolved tokens stream
+// through a 3-tile shared-memory ring (1 tile when K and V are separate buffers):
 //
-//   gather   warps 0-3   cp.async 16-byte copies of each token's 512-byte E4M3 latent row
+//   gather   warps 0-2   cp.async 16-byte copies of each token's 512-byte E4M3 latent row
 //                        (byte offsets resolved by the prologue; the next tile's offsets are
-//                        loaded while waiting for a free slot) into a 2-slot ring, written in
-//                        the 128-byte-swizzled K-major operand layout. (Per 512-byte row,
-//                        16-byte copies from 32 lanes sustain a higher gather rate on this
-//                        part than TMA tile::gather4 loads, whose per-instruction cost
-//                        limits an SM to about 17 GB/s.)
-//   QK^T     warp 4      tcgen05.mma kind::f8f6f4, M = 128 tokens, N = 128 (64 heads x
-//                        {hi, lo} query terms), K = 512: S^T -> TMEM (double buffered).
-//   softmax  warps 5-12  two warps per TMEM lane quarter, each thread one token and 32
-//                        heads: s = hi + lo, per-head scale, column max over the 128 tokens
-//                        (redux.sync.max per warp + a 4-way exchange), online rescale,
-//                        P' = 256*exp2(x - m) stored as two E4M3 terms (hi = top 4 bits,
-//                        lo = rest); the row sums stay per thread until the epilogue,
-//                        the running maxima in shared memory.
-//   P.V      warp 4      O^T[512 dims x 64 heads] += V^T * P'^T in TMEM: the same ring slot
-//                        read as an MN-major operand (K and V are the same bytes).
-//   epilogue warps 5-12  O / (256 l) * v_scale -> BF16 output, or (O/l, lse) partials,
-//                        transposed per warp through shared memory into 16-byte stores.
+//                        loaded while waiting for a free slot), written in the 128-byte-
+//                        swizzled operand layout, 8 tokens (4 KB) per swizzle group.
+//   QK^T     warp 3      tcgen05.mma kind::f8f6f4, M = 128 query rows (64 heads x {hi, lo}
+//                        terms, A in tensor memory), N = 128 tokens, K = 512: S -> TMEM.
+//   softmax  warps 4-11  the hi and lo rows of a head sit in neighbouring TMEM lanes, so
+//                        one shuffle gives each thread the full scores of one head for 32
+//                        tokens. A head's reference max is raised only when a tile exceeds
+//                        it by more than kRescaleMargin (one barrier-reduction per tile
+//                        decides for the CTA); then O is rescaled in TMEM. P' =
+//                        2^(x - m + kPBias) is stored as two E4M3 terms (hi = top 4 bits,
+//                        lo = rest).
+//   P.V      warp 3      O^T[512 dims x 64 heads] += V^T * P'^T in TMEM: the ring slot read
+//                        as an MN-major operand (K and V are the same bytes).
+//   epilogue warps 4-11  O / l * v_scale -> BF16 output, or (O/l, lse) partials, transposed
+//                        per warp through shared memory into 16-byte stores.
 //
 // The contraction is exact in its inputs: keys and values are the cached E4M3 codes
 // themselves (k_scale and v_scale are applied outside the MMA), queries are split into
 // two E4M3 terms that reproduce the BF16 value (see prologue.cu), probabilities into two
 // terms that carry about 8 significant bits. Accumulation is FP32 in TMEM.
 //
-// Shared memory 212 KB, TMEM 512 columns: O^T at 0..255 (chunk c of 128 dims at 64c),
-// S^T buffers at 256 and 384. Every wait is bounded (see ptx.cuh); on a timeout the CTA
-// records DSA_ERR_TIMEOUT, skips the remaining waits and finishes.
+// Shared memory 211 KB, TMEM 512 columns: O^T at 0..255 (chunk c of 128 dims at 64c),
+// query operand at 256..383, S at 384..511. Every wait is bounded (see ptx.cuh); on a
+// timeout the CTA records DSA_ERR_TIMEOUT, skips the remaining waits and finishes.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -42,48 +41,62 @@
 namespace dsa {
 namespace {
 
-constexpr int kProducerWarps = 4;
-constexpr int kMmaWarp = 4;
-constexpr int kSoftmaxWarp0 = 5;
+constexpr int kProducerWarps = 3;
+constexpr int kMmaWarp = 3;
+constexpr int kSoftmaxWarp0 = 4;
 constexpr int kSoftmaxWarps = 8;
-constexpr int kThreads = (kSoftmaxWarp0 + kSoftmaxWarps) * 32;  // 416
-constexpr int kProducerThreads = kProducerWarps * 32;
+constexpr int kThreads = (kSoftmaxWarp0 + kSoftmaxWarps) * 32;  // 384: 3 warps per SM sub-partition
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
+constexpr int kQuarters = kTileTokens / 32;  // a tile is gathered as 4 quarters of 32 tokens
 
-// Named barriers (0 is __syncthreads): one per head half of the softmax warps, one for
-// all softmax warps.
-constexpr int kBarHalf0 = 1;
-constexpr int kBarSoftmax = 3;
+constexpr int kBarSoftmax = 1;  // named barrier over the softmax warps
 
+// Operand layout of a tile: token tk at (tk/8)*4096 + kb*1024 + (tk%8)*128 for its
+// 128-dim block kb, 16-byte chunks of each 128-byte row permuted by tk%8 (128-byte
+// swizzle); 8-token groups are the swizzle atoms (stride kGroupBytes).
+constexpr int kGroupBytes = 8 * kLatent;  // 4 KB
+constexpr int kRingBytes = 3 * kKvTileBytes;                     // 192 KB
+constexpr int kPTermBytes = kHeadsPerCta * kTileTokens;          // 8 KB
 constexpr int kOffRing = 0;
-constexpr int kOffQ = 2 * kKvTileBytes;
-constexpr int kOffP = kOffQ + kQImageBytes;              // P' hi (8 KB) then lo (8 KB)
-constexpr int kPTermBytes = kTileTokens * kHeadsPerCta;  // 8 KB
-constexpr int kOffRed = kOffP + 2 * kPTermBytes;         // float [2 parity][4 quarters][64 heads]
-constexpr int kOffCs = kOffRed + 2 * 4 * kHeadsPerCta * 4;
-constexpr int kOffM = kOffCs + kHeadsPerCta * 4;         // float [2 parity][64 heads] running max
-constexpr int kOffBars = kOffM + 2 * kHeadsPerCta * 4;
+constexpr int kOffP = kOffRing + kRingBytes;                     // P' hi, lo; epilogue staging
+constexpr int kOffHm = kOffP + 2 * kPTermBytes;                  // float [2 token halves][64] tile maxima
+constexpr int kOffAlpha = kOffHm + 2 * kHeadsPerCta * 4;         // float [64] rescale factors
+constexpr int kOffL = kOffAlpha + kHeadsPerCta * 4;              // float [2 token halves][64] row sums
+constexpr int kOffF = kOffL + 2 * kHeadsPerCta * 4;              // float [64] output factors
+constexpr int kOffBars = kOffF + kHeadsPerCta * 4;
 enum {
-    BAR_FULL0, BAR_FULL1, BAR_EMPTY0, BAR_EMPTY1, BAR_SFULL0, BAR_SFULL1, BAR_SEMPTY0, BAR_SEMPTY1,
-    BAR_PFULL, BAR_PVDONE, BAR_QFULL, BAR_QEMPTY, BAR_OEMPTY, BAR_DRAIN, BAR_DONE, kNumBars
+    BAR_FULL0 = 0,   // 3: ring slot gathered
+    BAR_EMPTY0 = 3,  // 3: ring slot free again (its P.V is done)
+    BAR_SFULL = 6,   // S written by QK
+    BAR_SEMPTY,      // S read by the softmax warps
+    BAR_PFULL,       // P written
+    BAR_PVDONE,      // P.V done
+    BAR_QFULL,
+    BAR_QEMPTY,
+    BAR_OEMPTY,
+    BAR_DRAIN,
+    BAR_DONE,
+    kNumBars
 };
 constexpr int kOffTmemSlot = kOffBars + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
 constexpr int kSmemUsed = kOffAbort + 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for the 1024-byte alignment
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;
-constexpr uint32_t kTmemS = 256;
+constexpr uint32_t kTmemQ = 256;
+constexpr uint32_t kTmemS = 384;
 
 constexpr float kNegInf = -__builtin_huge_valf();
 
 // Optional per-CTA timeline (clock64 values), compiled in only with -DDSA_TRACE: slot i of
-// CTA c is trace[c*64 + i].
+// CTA c is trace[c*128 + i].
 #ifdef DSA_TRACE
-#define DSA_TRACE_AT(p, i)                                                                             \
-    do {                                                                                               \
-        if ((p).trace && (i) < 64) (p).trace[static_cast<int64_t>(blockIdx.x) * 64 + (i)] = clock64(); \
+#define DSA_TRACE_AT(p, i)                                                                               \
+    do {                                                                                                 \
+        if ((p).trace && (i) < 128) (p).trace[static_cast<int64_t>(blockIdx.x) * 128 + (i)] = clock64(); \
     } while (0)
 #else
 #define DSA_TRACE_AT(p, i) \
@@ -121,20 +134,6 @@ __device__ __forceinline__ void warp_wait(const DecodeParams& p, uint32_t bar, u
     __syncwarp();
 }
 
-// Barrier over the four softmax warps that share a head half.
-__device__ __forceinline__ void half_bar_sync(int hh) {
-    if (hh == 0)
-        named_bar_sync<kBarHalf0, 128>();
-    else
-        named_bar_sync<kBarHalf0 + 1, 128>();
-}
-
-__device__ __forceinline__ float redux_max(float x) {
-    float r;
-    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
-    return r;
-}
-
 __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
     return f32x2_to_e4m3x2(a, b) | (f32x2_to_e4m3x2(c, d) << 16);
 }
@@ -152,68 +151,82 @@ __device__ __forceinline__ void griddep_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Ring geometry: with K and V in one buffer each of the 3 slots holds one tile; otherwise
+// the single slot holds a K tile followed by the V tile.
+struct Ring {
+    int slots;
+    uint32_t slot_bytes;
+    __device__ explicit Ring(int kv_same)
+        : slots(kv_same ? 3 : 1), slot_bytes(kv_same ? kKvTileBytes : 2 * kKvTileBytes) {}
+};
+
 // ------------------------------------------------------------------------------------
 // gather warps
 // ------------------------------------------------------------------------------------
 __device__ void run_producer(const DecodeParams& p, uint32_t sbase, volatile int* abort_flag, int nseg) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nslot = p.kv_same ? 2 : 1;
+    const Ring ring(p.kv_same);
     const int64_t W = p.part.width;
-    const uint32_t chunk = (lane >> 3) * kKBlockBytes;  // K-block of this lane's 16-byte chunk
-    uint32_t tau = 0;
-    int qseg = 0;
+    // Quarters (32 tokens) of the CTA's tiles, numbered 4*tau + quarter across all its
+    // units, go round-robin to the gather warps: this warp takes numbers = warp mod 3.
+    uint32_t tau0 = 0;  // first tile of the current unit
     for (int i = 0; i < nseg; ++i) {
         const Segment s = cta_segment(p.part, blockIdx.x, i);
         const Tiles tl = segment_tokens(p, s);
         if (tl.n <= 0) continue;
-        if (tid == 0) {
-            if (qseg > 0 && !mbar_wait(sbase + kOffBars + 8 * BAR_QEMPTY, (qseg - 1) & 1, abort_flag))
-                fail(p, abort_flag, kStatusTimeout);
-            const uint32_t qbar = sbase + kOffBars + 8 * BAR_QFULL;
-            mbar_arrive_expect_tx(qbar, kQImageBytes);
-            const uint8_t* src = p.qimg + static_cast<int64_t>(s.unit) * kQImageBytes;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) bulk_g2s(sbase + kOffQ + k * 16384, src + k * 16384, 16384, qbar);
-            if (qseg == 0) DSA_TRACE_AT(p, 3);
-        }
-        __syncwarp();
-        ++qseg;
         const long long* offs = p.offs + static_cast<int64_t>(s.row) * W + tl.t0;
-        const int tok = warp * 32 + lane;  // this lane's token of each tile
-        long long nx = tok < tl.n ? offs[tok] : -1;
-        for (int t = 0; t < tl.ntiles; ++t, ++tau) {
+        const uint32_t g_end = (tau0 + tl.ntiles) * kQuarters;
+        uint32_t g = tau0 * kQuarters;
+        g += (static_cast<uint32_t>(warp) + kProducerWarps - g % kProducerWarps) % kProducerWarps;
+        // this lane's token of quarter g (segment-relative), its byte offset prefetched
+        auto tok_of = [&](uint32_t gq) { return static_cast<int32_t>((gq - tau0 * kQuarters) * 32) + lane; };
+        long long nx = -1;
+        if (g < g_end) nx = tok_of(g) < tl.n ? offs[tok_of(g)] : -1;
+        for (; g < g_end; g += kProducerWarps) {
             const long long o_mine = nx;
-            const int32_t next = (t + 1) * kTileTokens + tok;
-            if (t + 1 < tl.ntiles) nx = next < tl.n ? offs[next] : -1;  // before the slot wait
-            if (t * kTileTokens + tok < tl.n && o_mine < 0) atomicCAS(p.status, 0, kStatusBounds);
-            const int slot = static_cast<int>(tau % nslot);
-            const uint32_t use = tau / nslot;
-            if (tau >= static_cast<uint32_t>(nslot))
-                warp_wait(p, sbase + kOffBars + 8 * (BAR_EMPTY0 + slot), (use - 1) & 1, abort_flag);
-            if (tid == 0 && tau < 8) DSA_TRACE_AT(p, 40 + tau);
-            const uint32_t kdst = sbase + kOffRing + slot * kKvTileBytes;
-            const uint32_t vdst = p.kv_same ? kdst : sbase + kOffRing + kKvTileBytes;
+            const int32_t tok = tok_of(g);
+            const uint32_t gn = g + kProducerWarps;
+            if (gn < g_end) nx = tok_of(gn) < tl.n ? offs[tok_of(gn)] : -1;  // before the slot wait
+            if (tok < tl.n && o_mine < 0) atomicCAS(p.status, 0, kStatusBounds);
+            const uint32_t tau = g / kQuarters;
+            const int qq = static_cast<int>(g % kQuarters);
+            const int e = static_cast<int>(tau % ring.slots);
+            const uint32_t use = tau / ring.slots;
+            if (tau >= static_cast<uint32_t>(ring.slots))
+                warp_wait(p, sbase + kOffBars + 8 * (BAR_EMPTY0 + e), (use - 1) & 1, abort_flag);
+            if (lane == 0 && qq == 0 && tau < 8) DSA_TRACE_AT(p, 40 + tau);
+            const uint32_t kdst = sbase + kOffRing + e * ring.slot_bytes;
+            const uint32_t vdst = kdst + kKvTileBytes;
+            // Branch-free copy loop (a branch on the shuffled offset would serialise the
+            // copies): rows without a token (o < 0) are zero-filled by a source size of 0.
+            if (p.kv_same) {
+#pragma unroll 8
+                for (int j = 0; j < 32; ++j) {
+                    const long long o = __shfl_sync(0xffffffffu, o_mine, j);
+                    const int tk = qq * 32 + j;
+                    const uint32_t d = (tk >> 3) * kGroupBytes + (lane >> 3) * 1024 + (tk & 7) * 128 +
+                                       (((lane & 7) ^ (tk & 7)) << 4);
+                    cp_async_16_zfill(kdst + d, p.k_cache + (o >= 0 ? o : 0) + lane * 16, o >= 0 ? 16u : 0u);
+                }
+            } else {
 #pragma unroll 4
-            for (int j = 0; j < 32; ++j) {
-                const long long o = __shfl_sync(0xffffffffu, o_mine, j);
-                const int tk = warp * 32 + j;
-                const uint32_t d = chunk + tk * 128 + (((lane & 7) ^ (tk & 7)) << 4);
-                if (o >= 0) {
-                    cp_async_16(kdst + d, p.k_cache + o + lane * 16);
-                    if (!p.kv_same) cp_async_16(vdst + d, p.v_cache + o + lane * 16);
-                } else {
-                    st_shared_v4(kdst + d, 0u, 0u, 0u, 0u);
-                    if (!p.kv_same) st_shared_v4(vdst + d, 0u, 0u, 0u, 0u);
+                for (int j = 0; j < 32; ++j) {
+                    const long long o = __shfl_sync(0xffffffffu, o_mine, j);
+                    const int tk = qq * 32 + j;
+                    const uint32_t d = (tk >> 3) * kGroupBytes + (lane >> 3) * 1024 + (tk & 7) * 128 +
+                                       (((lane & 7) ^ (tk & 7)) << 4);
+                    const uint32_t n = o >= 0 ? 16u : 0u;
+                    cp_async_16_zfill(kdst + d, p.k_cache + (o >= 0 ? o : 0) + lane * 16, n);
+                    cp_async_16_zfill(vdst + d, p.v_cache + (o >= 0 ? o : 0) + lane * 16, n);
                 }
             }
-            const uint32_t fb = sbase + kOffBars + 8 * (BAR_FULL0 + slot);
+            const uint32_t fb = sbase + kOffBars + 8 * (BAR_FULL0 + e);
             cp_async_arrive_noinc(fb);
             mbar_arrive(fb);
-            if (tid == 0 && tau == 0) DSA_TRACE_AT(p, 4);
-            if (tid == 0 && tau < 8) DSA_TRACE_AT(p, 48 + tau);
+            if (lane == 0 && qq == kQuarters - 1 && tau < 8) DSA_TRACE_AT(p, 48 + tau);
         }
+        tau0 += tl.ntiles;
     }
-    if (tid == 0) DSA_TRACE_AT(p, 5);
     cp_async_wait_all();
 }
 
@@ -221,56 +234,66 @@ __device__ void run_producer(const DecodeParams& p, uint32_t sbase, volatile int
 // MMA warp (one thread issues)
 // ------------------------------------------------------------------------------------
 __device__ void run_mma(const DecodeParams& p, uint32_t sbase, uint32_t tmem, volatile int* abort_flag, int nseg) {
-    const int nslot = p.kv_same ? 2 : 1;
-    const uint32_t idq = idesc_e4m3(128, 128, false, false);
-    const uint32_t idp = idesc_e4m3(128, 64, true, true);
+    const Ring ring(p.kv_same);
+    const uint32_t idq = idesc_e4m3(128, kTileTokens, false, false);
+    const uint32_t idp = idesc_e4m3(128, kHeadsPerCta, true, false);
     auto barp = [&](int b) { return sbase + kOffBars + 8 * b; };
     uint32_t tau = 0;
     int qseg = 0;
 
+    // Descriptors are formed once per tile and stepped by immediate offsets (the start
+    // address field counts 16-byte units), keeping the issue loop short: the issuing
+    // thread shares its scheduler with two softmax warps, and a slow issue would leave
+    // the tensor core idle.
+    const uint64_t pdesc = smem_desc(sbase + kOffP, 1024, 128, kSwizzleNone);
     auto issue_pv = [&](uint32_t tp, bool first) {
         if (!mbar_wait(barp(BAR_PFULL), tp & 1, abort_flag)) fail(p, abort_flag, kStatusTimeout);
-        if (tp == 0) DSA_TRACE_AT(p, 9);
         if (first && qseg > 0 && !mbar_wait(barp(BAR_OEMPTY), (qseg - 1) & 1, abort_flag))
             fail(p, abort_flag, kStatusTimeout);
         tc_fence_after();
-        const int slot = static_cast<int>(tp % nslot);
-        const uint32_t vbase = sbase + kOffRing + (p.kv_same ? slot * kKvTileBytes : kKvTileBytes);
+        const int e = static_cast<int>(tp % ring.slots);
+        const uint32_t vbase = sbase + kOffRing + e * ring.slot_bytes + (p.kv_same ? 0u : kKvTileBytes);
+        // V^T: 128 dims of block mc x 32 tokens (4 swizzle groups), MN-major. P'^T: 64 heads
+        // x 32 tokens, K-major core matrices (token chunk stride 1 KB, head group 128 B).
+        const uint64_t vdesc = smem_desc(vbase, 1024, kGroupBytes, kSwizzle128B);
 #pragma unroll
         for (int mc = 0; mc < 4; ++mc) {
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t a = smem_desc(vbase + mc * kKBlockBytes + ks * 4096, kKBlockBytes, 1024, kSwizzle128B);
-                const uint64_t bh = smem_desc(sbase + kOffP + ks * 512, 128, 2048, kSwizzleNone);
-                const uint64_t bl = smem_desc(sbase + kOffP + kPTermBytes + ks * 512, 128, 2048, kSwizzleNone);
-                mma_e4m3(tmem + kTmemO + mc * 64, a, bh, idp, (first && ks == 0) ? 0u : 1u);
-                mma_e4m3(tmem + kTmemO + mc * 64, a, bl, idp, 1u);
+            for (int ks = 0; ks < kTileTokens / 32; ++ks) {
+                const uint64_t a = vdesc + static_cast<uint64_t>((ks * 4 * kGroupBytes + mc * 1024) >> 4);
+                const uint64_t bh = pdesc + static_cast<uint64_t>((ks * 2048) >> 4);
+                const uint64_t bl = pdesc + static_cast<uint64_t>((kPTermBytes + ks * 2048) >> 4);
+                const uint32_t d = tmem + kTmemO + mc * 64;
+                if (ks == 0)
+                    mma_e4m3(d, a, bh, idp, first ? 0u : 1u);
+                else
+                    mma_e4m3_acc(d, a, bh, idp);
+                mma_e4m3_acc(d, a, bl, idp);
             }
         }
         tc_commit(barp(BAR_PVDONE));
-        tc_commit(barp(BAR_EMPTY0 + slot));
+        tc_commit(barp(BAR_EMPTY0 + e));
     };
 
     auto issue_qk = [&](uint32_t tq) {
-        const int slot = static_cast<int>(tq % nslot);
-        const int sb = tq & 1;
+        const int e = static_cast<int>(tq % ring.slots);
         fence_proxy_async_smem();
         tc_fence_after();
-        const uint32_t kbase = sbase + kOffRing + slot * kKvTileBytes;
+        // K: 128 tokens x 32 dims of block ks/4, K-major (8-token group stride 4 KB).
+        const uint64_t kdesc = smem_desc(sbase + kOffRing + e * ring.slot_bytes, 16, kGroupBytes, kSwizzle128B);
+        const uint32_t d = tmem + kTmemS;
+        mma_e4m3_ta(d, tmem + kTmemQ, kdesc, idq, 0u);
 #pragma unroll
-        for (int ks = 0; ks < 16; ++ks) {
-            const uint32_t off = (ks >> 2) * kKBlockBytes + (ks & 3) * 32;
-            mma_e4m3(tmem + kTmemS + sb * 128, smem_desc(kbase + off, 16, 1024, kSwizzle128B),
-                     smem_desc(sbase + kOffQ + off, 16, 1024, kSwizzle128B), idq, ks > 0 ? 1u : 0u);
-        }
-        tc_commit(barp(BAR_SFULL0 + sb));
-        if (tq == 0) DSA_TRACE_AT(p, 8);
+        for (int ks = 1; ks < 16; ++ks)
+            mma_e4m3_ta_acc(d, tmem + kTmemQ + ks * 8, kdesc + static_cast<uint64_t>(((ks >> 2) * 1024 + (ks & 3) * 32) >> 4),
+                            idq);
+        tc_commit(barp(BAR_SFULL));
     };
-    // Phase the QK of tile tq may start: its ring slot is full and its S buffer is free.
+    // QK of tile tq may start once its ring slot is full and S has been read.
     auto qk_ready = [&](uint32_t tq) {
-        const int slot = static_cast<int>(tq % nslot);
-        const bool full = mbar_try_wait(barp(BAR_FULL0 + slot), (tq / nslot) & 1);
-        return full && (tq < 2 || mbar_try_wait(barp(BAR_SEMPTY0 + (tq & 1)), ((tq >> 1) - 1) & 1));
+        const int e = static_cast<int>(tq % ring.slots);
+        const bool full = mbar_try_wait(barp(BAR_FULL0 + e), (tq / ring.slots) & 1);
+        return full && (tq == 0 || mbar_try_wait(barp(BAR_SEMPTY), (tq - 1) & 1));
     };
 
     for (int i = 0; i < nseg; ++i) {
@@ -278,16 +301,11 @@ __device__ void run_mma(const DecodeParams& p, uint32_t sbase, uint32_t tmem, vo
         const Tiles tl = segment_tokens(p, s);
         if (tl.n <= 0) continue;
         if (!mbar_wait(barp(BAR_QFULL), qseg & 1, abort_flag)) fail(p, abort_flag, kStatusTimeout);
-        if (qseg == 0) DSA_TRACE_AT(p, 6);
+        tc_fence_after();
         const uint32_t tau0 = tau;
-        // QK(t) and PV(t-1) are independent: issue whichever becomes ready first (with one
-        // ring slot, QK(t) needs the slot PV(t-1) frees, so PV(t-1) goes first).
+        // QK(t) and PV(t-1) are independent: issue whichever becomes ready first.
         for (int t = 0; t < tl.ntiles; ++t, ++tau) {
             bool qk_done = false, pv_done = (t == 0);
-            if (nslot == 1 && !pv_done) {
-                issue_pv(tau - 1, tau - 1 == tau0);
-                pv_done = true;
-            }
             const uint64_t t_start = globaltimer_ns();
             while (!qk_done || !pv_done) {
                 if (!qk_done && qk_ready(tau)) {
@@ -297,12 +315,22 @@ __device__ void run_mma(const DecodeParams& p, uint32_t sbase, uint32_t tmem, vo
                     qk_done = true;
                 }
                 if (!pv_done && mbar_try_wait(barp(BAR_PFULL), (tau - 1) & 1)) {
+                    if (tau - 1 < 8) DSA_TRACE_AT(p, 64 + tau - 1);
                     issue_pv(tau - 1, tau - 1 == tau0);
                     pv_done = true;
                 }
-                if ((!qk_done || !pv_done) && (*abort_flag || globaltimer_ns() - t_start > kWaitLimitNs)) {
-                    fail(p, abort_flag, kStatusTimeout);
-                    break;
+                if (!qk_done || !pv_done) {
+                    if (*abort_flag || globaltimer_ns() - t_start > kWaitLimitNs) {
+                        fail(p, abort_flag, kStatusTimeout);
+                        break;
+                    }
+                    // Sleep briefly on the barrier still awaited instead of spinning (the
+                    // spin would compete with the gather's copies for the memory pipe).
+                    if (!pv_done)
+                        mbar_try_wait_hint(barp(BAR_PFULL), (tau - 1) & 1, kPollHintNs);
+                    else
+                        mbar_try_wait_hint(barp(BAR_FULL0 + static_cast<int>(tau % ring.slots)),
+                                           (tau / ring.slots) & 1, kPollHintNs);
                 }
             }
         }
@@ -353,17 +381,23 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int sw = warp - kSoftmaxWarp0;      // 0..7
     const int q4 = warp & 3;                  // TMEM lane quarter of this warp
-    const int hh = sw >> 2;                   // head half: heads 32*hh .. 32*hh+31
-    const int h0 = hh * 32;
-    const int token = q4 * 32 + lane;         // token row of the tile = TMEM lane
+    const int half = sw >> 2;                 // token half of each tile: columns [64*half, 64*half + 64)
+    const int term = lane & 1;                // 0: hi row, 1: lo row
+    const int hq = 16 * q4 + (lane >> 1);     // head of this thread within the unit
     const int st = sw * 32 + lane;            // 0..255
-    float* red = reinterpret_cast<float*>(smem + kOffRed);   // [2][4][64]
-    float* c_s = reinterpret_cast<float*>(smem + kOffCs);
-    float* m_s = reinterpret_cast<float*>(smem + kOffM);     // [2][64]
-    uint8_t* stage = smem + kOffP + sw * 2048;               // epilogue staging (2 KB per warp)
+    float* hm_s = reinterpret_cast<float*>(smem + kOffHm);
+    float* alpha_s = reinterpret_cast<float*>(smem + kOffAlpha);
+    float* l_s = reinterpret_cast<float*>(smem + kOffL);
+    float* f_s = reinterpret_cast<float*>(smem + kOffF);
+    uint8_t* stage = smem + kOffP + sw * 2048;  // epilogue staging (2 KB per warp)
     auto barp = [&](int b) { return sbase + kOffBars + 8 * b; };
     const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
+    // This thread's first 16-byte row in a P' term buffer: K-major core matrices of 8 heads
+    // x 16 tokens, token chunk kc = 4*half + 2*term (+1 for the second), head group hq/8
+    // (chunk stride 1 KB, group stride 128 B).
+    const uint32_t p_off = ((4 * half + 2 * term) * 8 + (hq >> 3)) * 128 + (hq & 7) * 16;
     uint32_t tau = 0;
+    int qseg = 0;
 
     for (int i = 0; i < nseg; ++i) {
         const Segment s = cta_segment(p.part, blockIdx.x, i);
@@ -382,124 +416,140 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
             }
             continue;
         }
-        if (st < kHeadsPerCta) c_s[st] = p.qscale[static_cast<int64_t>(s.unit) * kHeadsPerCta + st];
-        named_bar_sync<kBarSoftmax, kSoftmaxThreads>();
-        if (st == 0 && i == 0) DSA_TRACE_AT(p, 12);
 
-        float l_part[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) l_part[k] = 0.0f;
-        for (int t = 0; t < tl.ntiles; ++t, ++tau) {
-            const int sb = tau & 1;
-            warp_wait(p, barp(BAR_SFULL0 + sb), (tau >> 1) & 1, abort_flag);
-            if (st == 0 && tau == 0) DSA_TRACE_AT(p, 13);
-            if (st == 0 && tau < 8) DSA_TRACE_AT(p, 24 + tau);
-            tc_fence_after();
-            float x[32];
-            {
-                const uint32_t ta = tmem + lane_base + kTmemS + sb * 128 + h0;
-                uint32_t a[32];
-                tmem_ld_x32(ta, a);        // hi-term scores of heads h0..h0+31
-#pragma unroll
-                for (int k = 0; k < 32; ++k) x[k] = __uint_as_float(a[k]);
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {  // lo-term scores, 16 columns at a time
-                    uint32_t b[16];
-                    tmem_ld_x16(ta + 64 + half * 16, b);
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) x[half * 16 + k] += __uint_as_float(b[k]);
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(barp(BAR_SEMPTY0 + sb));
-
-            const bool valid = t * kTileTokens + token < tl.n;
-#pragma unroll
-            for (int k = 0; k < 32; k += 4) {
-                const float4 c = *reinterpret_cast<const float4*>(c_s + h0 + k);
-                x[k] = valid ? x[k] * c.x : kNegInf;
-                x[k + 1] = valid ? x[k + 1] * c.y : kNegInf;
-                x[k + 2] = valid ? x[k + 2] * c.z : kNegInf;
-                x[k + 3] = valid ? x[k + 3] * c.w : kNegInf;
-            }
-            // Column max over this warp's 32 tokens, then over the 4 lane quarters.
-            float* rbuf = red + (tau & 1) * (4 * kHeadsPerCta);
-            {
-                float mine = kNegInf;
-#pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const float r = redux_max(x[k]);
-                    mine = (lane == k) ? r : mine;
-                }
-                rbuf[q4 * kHeadsPerCta + h0 + lane] = mine;
-            }
-            half_bar_sync(hh);
-            if (st == 0 && tau == 0) DSA_TRACE_AT(p, 14);
-            // Lane k owns head h0+k: tile max over the 4 quarters, running max (parity (t-1)&1
-            // in m_s, -inf before the first tile), new max and rescale factor alpha. The new max
-            // goes to parity t&1 (all four warps of the half write the same values), read back
-            // only after the next half barrier. Every lane then takes head k's values by
-            // shuffle as it uses them.
-            const int hk = h0 + lane;
-            const float mt = fmaxf(fmaxf(rbuf[hk], rbuf[kHeadsPerCta + hk]),
-                                   fmaxf(rbuf[2 * kHeadsPerCta + hk], rbuf[3 * kHeadsPerCta + hk]));
-            const float mo = t > 0 ? m_s[((t + 1) & 1) * kHeadsPerCta + hk] : kNegInf;
-            const float mn = fmaxf(mo, mt);
-            const float a_mine = (mo == kNegInf) ? 0.0f : ex2_approx(mo - mn);
-            m_s[(t & 1) * kHeadsPerCta + hk] = mn;
-            const uint32_t grew = __ballot_sync(0xffffffffu, a_mine < 1.0f);
-#pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                const float m_k = __shfl_sync(0xffffffffu, mn, k);
-                const float a_k = __shfl_sync(0xffffffffu, a_mine, k);
-                const float pr = ex2_approx(x[k] - m_k);
-                l_part[k] = l_part[k] * a_k + pr;
-                x[k] = pr;
-            }
-            // P and O may only change once the previous P.V has finished reading them.
-            if (t > 0) warp_wait(p, barp(BAR_PVDONE), (tau - 1) & 1, abort_flag);
+        // ---- query operand of this unit into TMEM (after the previous unit's last QK) ----
+        if (qseg > 0) warp_wait(p, barp(BAR_QEMPTY), (qseg - 1) & 1, abort_flag);
+        {
+            const uint4* src = reinterpret_cast<const uint4*>(
+                p.qimg + static_cast<int64_t>(s.unit) * kQImageBytes + (q4 * 32 + lane) * kLatent + half * 256);
 #pragma unroll
             for (int hc = 0; hc < 2; ++hc) {
-                uint32_t hw[4], lw[4];
+                uint32_t a[32];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    float ph[4], pl[4];
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 v = src[hc * 8 + c];
+                    a[4 * c] = v.x;
+                    a[4 * c + 1] = v.y;
+                    a[4 * c + 2] = v.z;
+                    a[4 * c + 3] = v.w;
+                }
+                tmem_st_x32(tmem + lane_base + kTmemQ + half * 64 + hc * 32, a);
+            }
+            tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(barp(BAR_QFULL));
+        const float c = p.qscale[static_cast<int64_t>(s.unit) * kHeadsPerCta + hq];
+        float m_ref = kNegInf;  // reference max of head hq (log2 units)
+        float l_part = 0.0f;    // this thread's share of the row sum of P'
+
+        for (int t = 0; t < tl.ntiles; ++t, ++tau) {
+            warp_wait(p, barp(BAR_SFULL), tau & 1, abort_flag);
+            if (st == 0 && tau < 8) DSA_TRACE_AT(p, 24 + tau);
+            tc_fence_after();
+            uint32_t va[32], vb[32];
+            tmem_ld_x32(tmem + lane_base + kTmemS + half * 64, va);
+            tmem_ld_x32(tmem + lane_base + kTmemS + half * 64 + 32, vb);
+            if (st == 0 && (tau == 2 || tau == 3)) DSA_TRACE_AT(p, 72 + 8 * (tau - 2));
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(barp(BAR_SEMPTY));
+
+            // Scores of head hq for tokens tok0 .. tok0+31: this lane's term plus the
+            // neighbouring lane's other term. The hi lane keeps the first 32 columns of its
+            // half, the lo lane the last 32.
+            const int tok0 = t * kTileTokens + half * 64 + term * 32;
+            float x[32];
+            bool over = false;
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float pp = x[hc * 16 + k * 4 + e] * kPScale;
-                        ph[e] = hi_part(pp);
-                        pl[e] = pp - ph[e];
+            for (int j = 0; j < 32; ++j) {
+                const float send = __uint_as_float(term ? va[j] : vb[j]);
+                const float mine = __uint_as_float(term ? vb[j] : va[j]);
+                const float other = __shfl_xor_sync(0xffffffffu, send, 1);
+                x[j] = (tok0 + j < tl.n) ? (mine + other) * c : kNegInf;
+                over |= x[j] > m_ref + kRescaleMargin;
+            }
+            const bool any_over = named_bar_any<kBarSoftmax, kSoftmaxThreads>(over);
+            if (st == 0 && (tau == 2 || tau == 3)) DSA_TRACE_AT(p, 73 + 8 * (tau - 2));
+            if (any_over) {
+                // Raise the reference max of every head whose tile max exceeds it by more
+                // than the margin; rescale O and the row sums by 2^(m_old - m_new).
+                float hmax = x[0];
+#pragma unroll
+                for (int j = 1; j < 32; ++j) hmax = fmaxf(hmax, x[j]);
+                hmax = fmaxf(hmax, __shfl_xor_sync(0xffffffffu, hmax, 1));
+                if (term == 0) hm_s[half * kHeadsPerCta + hq] = hmax;
+                named_bar_sync<kBarSoftmax, kSoftmaxThreads>();
+                if (st == 0 && (tau == 2 || tau == 3)) DSA_TRACE_AT(p, 77 + 8 * (tau - 2));
+                const float tm = fmaxf(hm_s[hq], hm_s[kHeadsPerCta + hq]);
+                const float m_new = tm > m_ref + kRescaleMargin ? tm + kRescaleSlack : m_ref;
+                const float alpha = m_ref == kNegInf ? 0.0f : ex2_approx(m_ref - m_new);
+                l_part *= alpha;
+                m_ref = m_new;
+                if (term == 0 && half == 0) alpha_s[hq] = alpha;
+                named_bar_sync<kBarSoftmax, kSoftmaxThreads>();
+                if (t > 0) {
+                    float amin = 1.0f;
+#pragma unroll
+                    for (int h = 0; h < kHeadsPerCta; h += 4) {
+                        const float4 a4 = *reinterpret_cast<const float4*>(alpha_s + h);
+                        amin = fminf(amin, fminf(fminf(a4.x, a4.y), fminf(a4.z, a4.w)));
                     }
-                    hw[k] = pack_e4m3x4(ph[0], ph[1], ph[2], ph[3]);
-                    lw[k] = pack_e4m3x4(pl[0], pl[1], pl[2], pl[3]);
-                }
-                const uint32_t off = (2 * hh + hc) * 2048 + token * 16;
-                st_shared_v4(sbase + kOffP + off, hw[0], hw[1], hw[2], hw[3]);
-                st_shared_v4(sbase + kOffP + kPTermBytes + off, lw[0], lw[1], lw[2], lw[3]);
-            }
-            if (t > 0 && grew != 0u) {
-                // Rescale this half's O^T columns by alpha (1 for heads whose max held).
-                float al[32];
-#pragma unroll
-                for (int k = 0; k < 32; ++k) al[k] = __shfl_sync(0xffffffffu, a_mine, k);
-                tc_fence_after();
+                    if (amin < 1.0f) {
+                        // O^T columns are heads: this warp rescales its lanes of chunks
+                        // 2*half and 2*half + 1, once the P.V before this tile is done.
+                        warp_wait(p, barp(BAR_PVDONE), (tau - 1) & 1, abort_flag);
+                        tc_fence_after();
 #pragma unroll 1
-                for (int mc = 0; mc < 4; ++mc) {
-                    const uint32_t ta = tmem + lane_base + kTmemO + mc * 64 + h0;
-                    uint32_t v[32];
-                    tmem_ld_x32(ta, v);
+                        for (int mc2 = 0; mc2 < 2; ++mc2) {
+#pragma unroll 1
+                            for (int hh = 0; hh < 2; ++hh) {
+                                const uint32_t ta = tmem + lane_base + kTmemO + (2 * half + mc2) * 64 + hh * 32;
+                                uint32_t o[32];
+                                tmem_ld_x32(ta, o);
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * al[k]);
-                    tmem_st_x32(ta, v);
+                                for (int k = 0; k < 32; ++k)
+                                    o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha_s[hh * 32 + k]);
+                                tmem_st_x32(ta, o);
+                            }
+                        }
+                        tmem_wait_st();
+                    }
                 }
-                tmem_wait_st();
             }
+
+            // P' = 2^(x - m + kPBias) as two E4M3 terms, 16 tokens per 16-byte row.
+            uint32_t hw[8], lw[8];
+            float lsum = 0.0f;
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+                float ph[4], pl[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float pp = ex2_approx(x[4 * g + e] - m_ref + kPBias);
+                    lsum += pp;
+                    ph[e] = hi_part(pp);
+                    pl[e] = pp - ph[e];
+                }
+                hw[g] = pack_e4m3x4(ph[0], ph[1], ph[2], ph[3]);
+                lw[g] = pack_e4m3x4(pl[0], pl[1], pl[2], pl[3]);
+            }
+            l_part += lsum;
+            if (st == 0 && (tau == 2 || tau == 3)) DSA_TRACE_AT(p, 74 + 8 * (tau - 2));
+            // The P buffer is free once the previous tile's P.V has finished reading it.
+            if (tau >= 1) warp_wait(p, barp(BAR_PVDONE), (tau - 1) & 1, abort_flag);
+            if (st == 0 && (tau == 2 || tau == 3)) DSA_TRACE_AT(p, 75 + 8 * (tau - 2));
+            const uint32_t pb = sbase + kOffP;
+            st_shared_v4(pb + p_off, hw[0], hw[1], hw[2], hw[3]);
+            st_shared_v4(pb + p_off + 1024, hw[4], hw[5], hw[6], hw[7]);
+            st_shared_v4(pb + kPTermBytes + p_off, lw[0], lw[1], lw[2], lw[3]);
+            st_shared_v4(pb + kPTermBytes + p_off + 1024, lw[4], lw[5], lw[6], lw[7]);
             fence_proxy_async_smem();
+            if (st == 0 && (tau == 2 || tau == 3)) DSA_TRACE_AT(p, 76 + 8 * (tau - 2));
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(barp(BAR_PFULL));
-            if (st == 0 && tau == 0) DSA_TRACE_AT(p, 16);
             if (st == 0 && tau < 8) DSA_TRACE_AT(p, 32 + tau);
         }
 
@@ -507,63 +557,49 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
         warp_wait(p, barp(BAR_PVDONE), (tau - 1) & 1, abort_flag);
         if (st == 0 && i == 0) DSA_TRACE_AT(p, 17);
         tc_fence_after();
-        // Row sums: per head over the warp's 32 tokens (butterfly, result in every lane),
-        // then over the 4 lane quarters through shared memory.
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-            float v = l_part[k];
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-            l_part[k] = v;
-        }
-        if (st == 0 && i == 0) DSA_TRACE_AT(p, 2);
-        if (lane == 0) {
-#pragma unroll
-            for (int k = 0; k < 32; k += 4)
-                *reinterpret_cast<float4*>(red + q4 * kHeadsPerCta + h0 + k) =
-                    make_float4(l_part[k], l_part[k + 1], l_part[k + 2], l_part[k + 3]);
-        }
-        half_bar_sync(hh);
-        // Lane k: head h0+k's row sum, output factor and (for a partial) log-sum-exp.
+        const float lpair = l_part + __shfl_xor_sync(0xffffffffu, l_part, 1);
+        if (term == 0) l_s[half * kHeadsPerCta + hq] = lpair;
+        named_bar_sync<kBarSoftmax, kSoftmaxThreads>();
         const bool whole = s.part < 0;
-        float f_mine;
-        {
-            const int hk = h0 + lane;
-            const float l = (red[hk] + red[kHeadsPerCta + hk]) + (red[2 * kHeadsPerCta + hk] + red[3 * kHeadsPerCta + hk]);
-            f_mine = (whole ? p.v_scale : 1.0f) / (kPScale * l);
-            if (!whole && q4 == 0)
-                p.part_lse[s.part * kHeadsPerCta + hk] = m_s[((tl.ntiles - 1) & 1) * kHeadsPerCta + hk] + __log2f(l);
+        if (term == 0 && half == 0) {
+            const float l = l_s[hq] + l_s[kHeadsPerCta + hq];
+            f_s[hq] = (whole ? p.v_scale : 1.0f) / l;
+            if (!whole) p.part_lse[s.part * kHeadsPerCta + hq] = m_ref + __log2f(l);
         }
-        float f[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) f[k] = __shfl_sync(0xffffffffu, f_mine, k);
-        if (st == 0 && i == 0) DSA_TRACE_AT(p, 15);
+        named_bar_sync<kBarSoftmax, kSoftmaxThreads>();
 #pragma unroll 1
-        for (int mc = 0; mc < 4; ++mc) {
-            uint32_t v[32];
-            tmem_ld_x32(tmem + lane_base + kTmemO + mc * 64 + h0, v);
-            float o[32];
-#pragma unroll
-            for (int k = 0; k < 32; ++k) o[k] = __uint_as_float(v[k]);
+        for (int mc2 = 0; mc2 < 2; ++mc2) {
+            const int mc = 2 * half + mc2;
             const int dim0 = mc * 128 + q4 * 32;
-            if (whole) {
-                __nv_bfloat16* rows = reinterpret_cast<__nv_bfloat16*>(p.out) + head0 * kLatent;
-                store_block(rows, h0, hvalid, dim0, o, f, stage, lane);
-                store_block(rows, h0 + 16, hvalid, dim0, o + 16, f + 16, stage, lane);
-            } else {
-                __half* rows = reinterpret_cast<__half*>(p.part_o) + static_cast<int64_t>(s.part) * kHeadsPerCta * kLatent;
-                store_block(rows, h0, kHeadsPerCta, dim0, o, f, stage, lane);
-                store_block(rows, h0 + 16, kHeadsPerCta, dim0, o + 16, f + 16, stage, lane);
+#pragma unroll 1
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t v[32];
+                tmem_ld_x32(tmem + lane_base + kTmemO + mc * 64 + hh * 32, v);
+                float o[32], f[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    o[k] = __uint_as_float(v[k]);
+                    f[k] = f_s[hh * 32 + k];
+                }
+                if (whole) {
+                    __nv_bfloat16* rows = reinterpret_cast<__nv_bfloat16*>(p.out) + head0 * kLatent;
+                    store_block(rows, hh * 32, hvalid, dim0, o, f, stage, lane);
+                    store_block(rows, hh * 32 + 16, hvalid, dim0, o + 16, f + 16, stage, lane);
+                } else {
+                    __half* rows = reinterpret_cast<__half*>(p.part_o) + static_cast<int64_t>(s.part) * kHeadsPerCta * kLatent;
+                    store_block(rows, hh * 32, kHeadsPerCta, dim0, o, f, stage, lane);
+                    store_block(rows, hh * 32 + 16, kHeadsPerCta, dim0, o + 16, f + 16, stage, lane);
+                }
             }
-            if (st == 0 && i == 0 && mc == 0) DSA_TRACE_AT(p, 23);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(barp(BAR_OEMPTY));
         if (st == 0 && i == 0) DSA_TRACE_AT(p, 18);
-        // The staging area is the P buffer, and c_s / red are reused: the next segment
-        // starts only after every softmax warp is done here.
+        // The staging area is the P buffer and l_s / f_s are reused: the next unit starts
+        // only after every softmax warp is done here.
         named_bar_sync<kBarSoftmax, kSoftmaxThreads>();
+        ++qseg;
     }
     if (st == 0) DSA_TRACE_AT(p, 19);
 }
@@ -578,18 +614,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
 
     if (tid == 0) {
         const uint32_t b = sbase + kOffBars;
-        // one cp.async arrival and one plain arrival per gather thread
-        mbar_init(b + 8 * BAR_FULL0, 2 * kProducerThreads);
-        mbar_init(b + 8 * BAR_FULL1, 2 * kProducerThreads);
-        mbar_init(b + 8 * BAR_EMPTY0, 1);
-        mbar_init(b + 8 * BAR_EMPTY1, 1);
-        mbar_init(b + 8 * BAR_SFULL0, 1);
-        mbar_init(b + 8 * BAR_SFULL1, 1);
-        mbar_init(b + 8 * BAR_SEMPTY0, kSoftmaxWarps);
-        mbar_init(b + 8 * BAR_SEMPTY1, kSoftmaxWarps);
+        for (int e = 0; e < 3; ++e) {
+            // one cp.async arrival and one plain arrival per lane of each quarter
+            mbar_init(b + 8 * (BAR_FULL0 + e), 2 * 32 * kQuarters);
+            mbar_init(b + 8 * (BAR_EMPTY0 + e), 1);
+        }
+        mbar_init(b + 8 * BAR_SFULL, 1);
+        mbar_init(b + 8 * BAR_SEMPTY, kSoftmaxWarps);
         mbar_init(b + 8 * BAR_PFULL, kSoftmaxWarps);
         mbar_init(b + 8 * BAR_PVDONE, 1);
-        mbar_init(b + 8 * BAR_QFULL, 1);
+        mbar_init(b + 8 * BAR_QFULL, kSoftmaxWarps);
         mbar_init(b + 8 * BAR_QEMPTY, 1);
         mbar_init(b + 8 * BAR_OEMPTY, kSoftmaxWarps);
         mbar_init(b + 8 * BAR_DRAIN, 1);
@@ -640,8 +674,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     tc_fence_before();
     __syncthreads();
     if (tid == 0) DSA_TRACE_AT(p, 20);
-    if (tid == kSoftmaxWarp0 * 32) DSA_TRACE_AT(p, 21);
-    if (tid == kMmaWarp * 32 + 1) DSA_TRACE_AT(p, 22);
     griddep_launch_dependents();
     if (warp == kMmaWarp) {
         tc_fence_after();
@@ -652,7 +684,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
 }  // namespace
 
 cudaError_t decode_kernel_setup() {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    // The register cap above must leave room for all kThreads threads of the block.
+    cudaFuncAttributes attr;
+    cudaError_t e = cudaFuncGetAttributes(&attr, decode_kernel);
+    if (e != cudaSuccess) return e;
+    if (attr.maxThreadsPerBlock < kThreads) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(decode_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
 }

@@ -11,11 +11,11 @@
 //   * longer rows: bitonic sort of the row in shared memory, then a prefix count of
 //     first occurrences.
 // Blocks [rows, rows + rows*groups) turn one (row, 64-head group) of BF16 queries into
-// the shared-memory image the decode kernel copies verbatim: per head a power-of-two
+// the operand image the decode kernel loads into tensor memory: per head a power-of-two
 // scale 2^e (|q|*2^e < 256) and two E4M3 terms hi + lo whose sum is q*2^e. hi keeps the
 // top 4 significant bits (truncation), lo is the remainder; for |q*2^e| >= 2^-2 the
-// split is exact, since a BF16 value has 8 significant bits. Rows 0..63 of the image
-// hold hi, rows 64..127 lo, in the K-major 128-byte-swizzled operand layout.
+// split is exact, since a BF16 value has 8 significant bits. The image is 128 rows of
+// 512 codes; row 32q + 2k + t holds term t of head 16q + k.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -213,14 +213,11 @@ __device__ void prepare_queries(const PrologueParams& p, int32_t unit) {
             hi[k] = f32x2_to_e4m3x2(vh[0], vh[1]) | (f32x2_to_e4m3x2(vh[2], vh[3]) << 16);
             lo[k] = f32x2_to_e4m3x2(vl[0], vl[1]) | (f32x2_to_e4m3x2(vl[2], vl[3]) << 16);
         }
-        // K-major SW128 image: K-block kb = lane/8 (128 dims), 16-byte chunk c = lane%8,
-        // row j stored at kb*16K + j*128 with its chunks permuted by j%8.
-        const int kb = lane >> 3, c = lane & 7;
-        const int jh = hl, jl = kHeadsPerCta + hl;
-        *reinterpret_cast<uint4*>(img + kb * kKBlockBytes + jh * 128 + ((c ^ (jh & 7)) << 4)) =
-            make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(img + kb * kKBlockBytes + jl * 128 + ((c ^ (jl & 7)) << 4)) =
-            make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        // Row-major image: rows 2k and 2k+1 of quarter q hold the hi and lo terms of head
+        // 16q + k, so the decode finds both terms of a head in neighbouring TMEM lanes.
+        const int rh = 32 * (hl >> 4) + 2 * (hl & 15);
+        *reinterpret_cast<uint4*>(img + rh * kLatent + lane * 16) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(img + (rh + 1) * kLatent + lane * 16) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         if (lane == 0)
             p.qscale[static_cast<int64_t>(unit) * kHeadsPerCta + hl] =
                 p.score_scale * __uint_as_float(static_cast<uint32_t>(127 - e) << 23);

@@ -64,6 +64,19 @@ __device__ __forceinline__ uint32_t mbar_try_wait_suspend(uint32_t bar, uint32_t
         : "memory");
     return ok;
 }
+// As mbar_try_wait, with the suspend hint given in nanoseconds.
+__device__ __forceinline__ uint32_t mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok;
+}
+constexpr uint32_t kPollHintNs = 500;
 // Waits for the phase with the given parity to complete. Returns false if the wait
 // ran out of time or the abort flag was raised meanwhile.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
@@ -81,6 +94,11 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
 // ------------------------------------------------------------------------------------
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// As cp_async_16, copying src_bytes (0 or 16) and filling the rest of the 16 bytes with
+// zeros; with src_bytes = 0 nothing is read from global memory.
+__device__ __forceinline__ void cp_async_16_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
 // The mbarrier receives one arrival when every cp.async this thread issued so far has
 // landed (counts toward the barrier's expected arrivals).
@@ -113,6 +131,23 @@ __device__ __forceinline__ void named_bar_sync() {
     static_assert(ID > 0 && ID < 16 && N % 32 == 0, "named barrier");
     __syncwarp();
     asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(N) : "memory");
+}
+
+// Named barrier ID over N threads that also returns whether `pred` held in any of them.
+template <int ID, int N>
+__device__ __forceinline__ bool named_bar_any(bool pred) {
+    static_assert(ID > 0 && ID < 16 && N % 32 == 0, "named barrier");
+    __syncwarp();
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, %2, %3, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"(pred ? 1u : 0u), "n"(ID), "n"(N)
+        : "memory");
+    return r != 0;
 }
 
 // ------------------------------------------------------------------------------------
@@ -149,6 +184,29 @@ __device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint6
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// As mma_e4m3 with the accumulate flag fixed to 1 (no predicate set-up per call).
+__device__ __forceinline__ void mma_e4m3_acc(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc) {
+    asm volatile("tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, 1;" ::"r"(d_tmem), "l"(a_desc), "l"(b_desc),
+                 "r"(idesc)
+                 : "memory");
+}
+__device__ __forceinline__ void mma_e4m3_ta_acc(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc) {
+    asm volatile("tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, 1;" ::"r"(d_tmem), "r"(a_tmem),
+                 "l"(b_desc), "r"(idesc)
+                 : "memory");
+}
+// As mma_e4m3, with A read from tensor memory (K-major: row i in lane i, four 8-bit K
+// elements per 32-bit column).
+__device__ __forceinline__ void mma_e4m3_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 

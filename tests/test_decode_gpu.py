@@ -217,6 +217,22 @@ def test_graph_capture_replay(api):
     assert torch.equal(out, want)
 
 
+def test_events_around_decode_kernel_outside_capture(api):
+    """The optional events bracket the decode kernel on the call's stream, captured or not."""
+    w = wl.random_case(num_seqs=2, heads=64, seq_len=3000, sel_width=1024, seed=15).to("cuda")
+    ws = api.alloc_workspace(2, 1, 64, 1024)
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    e1.record(s)                                   # creates both CUDA events
+    want = api.decode_workload(w, workspace=ws)
+    got = api.decode_workload(w, workspace=ws, ev_begin=e0, ev_end=e1)
+    torch.cuda.synchronize()
+    assert torch.equal(got, want)
+    assert e0.query() and e1.query()
+    assert e0.elapsed_time(e1) >= 0.0
+
+
 def test_bad_page_sets_device_status(api):
     w = wl.random_case(num_seqs=2, heads=8, seq_len=300, sel_width=100, hole_frac=0.0, dup_frac=0.0, seed=13)
     bt = w.block_tables.clone()
