@@ -28,7 +28,7 @@ constexpr int kResolveThreads = 256;
 // 2^(kPBias + kRescaleMargin) < 448, the E4M3 maximum, and rescales are rare.
 constexpr float kPBias = 7.0f;
 constexpr float kRescaleMargin = 1.75f;
-constexpr float kRescaleSlack = 2.0f;
+constexpr float kRescaleSlack = 3.0f;
 
 // Device status codes mirror dsa_status.
 constexpr int kStatusBounds = DSA_ERR_DEVICE_BOUNDS;

@@ -4,10 +4,11 @@
 // unit = (decode row, group of 64 query heads). Tiles of 128 resolved tokens stream
 // through a 3-tile shared-memory ring (1 tile when K and V are separate buffers):
 //
-//   gather   warps 0-2   cp.async 16-byte copies of each token's 512-byte E4M3 latent row
-//                        (byte offsets resolved by the prologue; the next tile's offsets are
-//                        loaded while waiting for a free slot), written in the 128-byte-
-//                        swizzled operand layout, 8 tokens (4 KB) per swizzle group.
+//   gather   warps 0-2   cp.async 16-byte copies of each token's 512-byte E4M3 latent row,
+//                        each warp a third of every tile (byte offsets resolved by the
+//                        prologue; the next tile's offsets are loaded while waiting for a
+//                        free slot), written in the 128-byte-swizzled operand layout, 8
+//                        tokens (4 KB) per swizzle group.
 //   QK^T     warp 3      tcgen05.mma kind::f8f6f4, M = 128 query rows (64 heads x {hi, lo}
 //                        terms, A in tensor memory), N = 128 tokens, K = 512: S -> TMEM.
 //   softmax  warps 4-11  the hi and lo rows of a head sit in neighbouring TMEM lanes, so
@@ -27,7 +28,7 @@
 // two E4M3 terms that reproduce the BF16 value (see prologue.cu), probabilities into two
 // terms that carry about 8 significant bits. Accumulation is FP32 in TMEM.
 //
-// Shared memory 211 KB, TMEM 512 columns: O^T at 0..255 (chunk c of 128 dims at 64c),
+// Shared memory 226 KB, TMEM 512 columns: O^T at 0..255 (chunk c of 128 dims at 64c),
 // query operand at 256..383, S at 384..511. Every wait is bounded (see ptx.cuh); on a
 // timeout the CTA records DSA_ERR_TIMEOUT, skips the remaining waits and finishes.
 #include <cuda_bf16.h>
@@ -47,7 +48,6 @@ constexpr int kSoftmaxWarp0 = 4;
 constexpr int kSoftmaxWarps = 8;
 constexpr int kThreads = (kSoftmaxWarp0 + kSoftmaxWarps) * 32;  // 384: 3 warps per SM sub-partition
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
-constexpr int kQuarters = kTileTokens / 32;  // a tile is gathered as 4 quarters of 32 tokens
 
 constexpr int kBarSoftmax = 1;  // named barrier over the softmax warps
 
@@ -55,23 +55,28 @@ constexpr int kBarSoftmax = 1;  // named barrier over the softmax warps
 // 128-dim block kb, 16-byte chunks of each 128-byte row permuted by tk%8 (128-byte
 // swizzle); 8-token groups are the swizzle atoms (stride kGroupBytes).
 constexpr int kGroupBytes = 8 * kLatent;  // 4 KB
-constexpr int kRingBytes = 3 * kKvTileBytes;                     // 192 KB
-constexpr int kPTermBytes = kHeadsPerCta * kTileTokens;          // 8 KB
+constexpr int kRingBytes = 192 * 1024;                           // ring of tiles (K == V)
+constexpr int kSlotsKV = kRingBytes / kKvTileBytes;              // tiles in flight when K == V
+constexpr int kSBufs = 128 / kTileTokens;                        // S buffers in TMEM columns 384..511
+constexpr int kHalfCols = kTileTokens / 2;                       // S columns per softmax warp
+constexpr int kScores = kHalfCols / 2;                           // scores per softmax thread per tile
+constexpr int kPTermBytes = kHeadsPerCta * kTileTokens;          // one E4M3 term of P'^T
+static_assert(kSlotsKV <= 6 && kSBufs >= 1 && kScores % 16 == 0, "tile geometry");
 constexpr int kOffRing = 0;
-constexpr int kOffP = kOffRing + kRingBytes;                     // P' hi, lo; epilogue staging
-constexpr int kOffHm = kOffP + 2 * kPTermBytes;                  // float [2 token halves][64] tile maxima
+constexpr int kOffP = kOffRing + kRingBytes;                     // P' [2 buffers][hi, lo]; epilogue staging
+constexpr int kOffHm = kOffP + 4 * kPTermBytes;                  // float [2 token halves][64] tile maxima
 constexpr int kOffAlpha = kOffHm + 2 * kHeadsPerCta * 4;         // float [64] rescale factors
 constexpr int kOffL = kOffAlpha + kHeadsPerCta * 4;              // float [2 token halves][64] row sums
 constexpr int kOffF = kOffL + 2 * kHeadsPerCta * 4;              // float [64] output factors
 constexpr int kOffBars = kOffF + kHeadsPerCta * 4;
 enum {
-    BAR_FULL0 = 0,   // 3: ring slot gathered
-    BAR_EMPTY0 = 3,  // 3: ring slot free again (its P.V is done)
-    BAR_SFULL = 6,   // S written by QK
-    BAR_SEMPTY,      // S read by the softmax warps
-    BAR_PFULL,       // P written
-    BAR_PVDONE,      // P.V done
-    BAR_QFULL,
+    BAR_FULL0 = 0,    // 6: ring slot gathered
+    BAR_EMPTY0 = 6,   // 6: ring slot free again (its P.V is done)
+    BAR_SFULL0 = 12,  // 2: S buffer written by QK
+    BAR_SEMPTY0 = 14, // 2: S buffer read by the softmax warps
+    BAR_PFULL0 = 16,  // 2: P buffer written
+    BAR_PVDONE0 = BAR_PFULL0 + 2,  // 2: the P.V reading a P buffer is done
+    BAR_QFULL = BAR_PVDONE0 + 2,
     BAR_QEMPTY,
     BAR_OEMPTY,
     BAR_DRAIN,
@@ -151,81 +156,89 @@ __device__ __forceinline__ void griddep_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Ring geometry: with K and V in one buffer each of the 3 slots holds one tile; otherwise
-// the single slot holds a K tile followed by the V tile.
+// Ring geometry: with K and V in one buffer each slot holds one tile; otherwise a slot
+// holds a K tile followed by the V tile.
 struct Ring {
     int slots;
     uint32_t slot_bytes;
     __device__ explicit Ring(int kv_same)
-        : slots(kv_same ? 3 : 1), slot_bytes(kv_same ? kKvTileBytes : 2 * kKvTileBytes) {}
+        : slots(kv_same ? kSlotsKV : kSlotsKV / 2), slot_bytes(kv_same ? kKvTileBytes : 2 * kKvTileBytes) {}
 };
 
 // ------------------------------------------------------------------------------------
 // gather warps
 // ------------------------------------------------------------------------------------
+// Rows of a tile taken by gather warp w: [w*43, min(w*43 + 43, 128)).
+constexpr int kWarpRows = (kTileTokens + kProducerWarps - 1) / kProducerWarps;
+
 __device__ void run_producer(const DecodeParams& p, uint32_t sbase, volatile int* abort_flag, int nseg) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const Ring ring(p.kv_same);
     const int64_t W = p.part.width;
-    // Quarters (32 tokens) of the CTA's tiles, numbered 4*tau + quarter across all its
-    // units, go round-robin to the gather warps: this warp takes numbers = warp mod 3.
-    uint32_t tau0 = 0;  // first tile of the current unit
+    const int r0 = warp * kWarpRows;
+    const int nr = min(kWarpRows, kTileTokens - r0);
+    uint32_t tau = 0;
     for (int i = 0; i < nseg; ++i) {
         const Segment s = cta_segment(p.part, blockIdx.x, i);
         const Tiles tl = segment_tokens(p, s);
         if (tl.n <= 0) continue;
         const long long* offs = p.offs + static_cast<int64_t>(s.row) * W + tl.t0;
-        const uint32_t g_end = (tau0 + tl.ntiles) * kQuarters;
-        uint32_t g = tau0 * kQuarters;
-        g += (static_cast<uint32_t>(warp) + kProducerWarps - g % kProducerWarps) % kProducerWarps;
-        // this lane's token of quarter g (segment-relative), its byte offset prefetched
-        auto tok_of = [&](uint32_t gq) { return static_cast<int32_t>((gq - tau0 * kQuarters) * 32) + lane; };
-        long long nx = -1;
-        if (g < g_end) nx = tok_of(g) < tl.n ? offs[tok_of(g)] : -1;
-        for (; g < g_end; g += kProducerWarps) {
-            const long long o_mine = nx;
-            const int32_t tok = tok_of(g);
-            const uint32_t gn = g + kProducerWarps;
-            if (gn < g_end) nx = tok_of(gn) < tl.n ? offs[tok_of(gn)] : -1;  // before the slot wait
-            if (tok < tl.n && o_mine < 0) atomicCAS(p.status, 0, kStatusBounds);
-            const uint32_t tau = g / kQuarters;
-            const int qq = static_cast<int>(g % kQuarters);
+        // This lane's rows of tile t: r0 + lane and r0 + 32 + lane (the latter for lane < nr - 32).
+        auto load = [&](int t, long long& a, long long& b) {
+            const int ta = t * kTileTokens + r0 + lane, tb = ta + 32;
+            a = (t < tl.ntiles && ta < tl.n) ? offs[ta] : -1;
+            b = (t < tl.ntiles && lane + 32 < nr && tb < tl.n) ? offs[tb] : -1;
+        };
+        long long oa, ob;
+        load(0, oa, ob);
+        for (int t = 0; t < tl.ntiles; ++t, ++tau) {
+            const long long ca = oa, cb = ob;
+            load(t + 1, oa, ob);  // next tile's rows, before the slot wait
+            if ((ca < 0 && t * kTileTokens + r0 + lane < tl.n) ||
+                (cb < 0 && lane + 32 < nr && t * kTileTokens + r0 + 32 + lane < tl.n))
+                atomicCAS(p.status, 0, kStatusBounds);
             const int e = static_cast<int>(tau % ring.slots);
             const uint32_t use = tau / ring.slots;
             if (tau >= static_cast<uint32_t>(ring.slots))
                 warp_wait(p, sbase + kOffBars + 8 * (BAR_EMPTY0 + e), (use - 1) & 1, abort_flag);
-            if (lane == 0 && qq == 0 && tau < 8) DSA_TRACE_AT(p, 40 + tau);
+            if (tid == 0 && tau < 8) DSA_TRACE_AT(p, 40 + tau);
             const uint32_t kdst = sbase + kOffRing + e * ring.slot_bytes;
             const uint32_t vdst = kdst + kKvTileBytes;
             // Branch-free copy loop (a branch on the shuffled offset would serialise the
             // copies): rows without a token (o < 0) are zero-filled by a source size of 0.
-            if (p.kv_same) {
+            // Each row's offset is broadcast from the lane holding it. Offsets below 64 GiB
+            // travel as 32-bit counts of 16-byte units (one shuffle per row; 0xFFFFFFFF marks
+            // a row without token); a tile with a larger offset takes the 64-bit path.
+            const uint8_t* kbase = p.k_cache + lane * 16;
+            const uint8_t* vbase = p.v_cache + lane * 16;
+            auto copy_row = [&](long long o, int tk) {
+                const uint32_t d = (tk >> 3) * kGroupBytes + (lane >> 3) * 1024 + (tk & 7) * 128 +
+                                   (((lane & 7) ^ (tk & 7)) << 4);
+                const bool ok = o >= 0;
+                const uint64_t src = ok ? static_cast<uint64_t>(o) : 0;
+                cp_async_16_zfill(kdst + d, kbase + src, ok ? 16u : 0u);
+                if (!p.kv_same) cp_async_16_zfill(vdst + d, vbase + src, ok ? 16u : 0u);
+            };
+            constexpr long long kNarrow = 1ll << 36;
+            if (!__any_sync(0xffffffffu, ca >= kNarrow || cb >= kNarrow)) {
+                auto to16 = [](long long o) { return o >= 0 ? static_cast<uint32_t>(o >> 4) : 0xFFFFFFFFu; };
+                auto from16 = [](uint32_t u) { return u != 0xFFFFFFFFu ? static_cast<long long>(u) << 4 : -1ll; };
+                const uint32_t ua = to16(ca), ub = to16(cb);
 #pragma unroll 8
-                for (int j = 0; j < 32; ++j) {
-                    const long long o = __shfl_sync(0xffffffffu, o_mine, j);
-                    const int tk = qq * 32 + j;
-                    const uint32_t d = (tk >> 3) * kGroupBytes + (lane >> 3) * 1024 + (tk & 7) * 128 +
-                                       (((lane & 7) ^ (tk & 7)) << 4);
-                    cp_async_16_zfill(kdst + d, p.k_cache + (o >= 0 ? o : 0) + lane * 16, o >= 0 ? 16u : 0u);
-                }
+                for (int j = 0; j < min(nr, 32); ++j) copy_row(from16(__shfl_sync(0xffffffffu, ua, j)), r0 + j);
+                if (kWarpRows > 32)
+                    for (int j = 32; j < nr; ++j) copy_row(from16(__shfl_sync(0xffffffffu, ub, j - 32)), r0 + j);
             } else {
 #pragma unroll 4
-                for (int j = 0; j < 32; ++j) {
-                    const long long o = __shfl_sync(0xffffffffu, o_mine, j);
-                    const int tk = qq * 32 + j;
-                    const uint32_t d = (tk >> 3) * kGroupBytes + (lane >> 3) * 1024 + (tk & 7) * 128 +
-                                       (((lane & 7) ^ (tk & 7)) << 4);
-                    const uint32_t n = o >= 0 ? 16u : 0u;
-                    cp_async_16_zfill(kdst + d, p.k_cache + (o >= 0 ? o : 0) + lane * 16, n);
-                    cp_async_16_zfill(vdst + d, p.v_cache + (o >= 0 ? o : 0) + lane * 16, n);
-                }
+                for (int j = 0; j < min(nr, 32); ++j) copy_row(__shfl_sync(0xffffffffu, ca, j), r0 + j);
+                if (kWarpRows > 32)
+                    for (int j = 32; j < nr; ++j) copy_row(__shfl_sync(0xffffffffu, cb, j - 32), r0 + j);
             }
-            const uint32_t fb = sbase + kOffBars + 8 * (BAR_FULL0 + e);
-            cp_async_arrive_noinc(fb);
-            mbar_arrive(fb);
-            if (lane == 0 && qq == kQuarters - 1 && tau < 8) DSA_TRACE_AT(p, 48 + tau);
+            // One arrival per lane, made when the lane's copies so far have landed (.noinc: the
+            // arrival counts toward the barrier's expected 96 per tile).
+            cp_async_arrive_noinc(sbase + kOffBars + 8 * (BAR_FULL0 + e));
+            if (tid == 0 && tau < 8) DSA_TRACE_AT(p, 48 + tau);
         }
-        tau0 += tl.ntiles;
     }
     cp_async_wait_all();
 }
@@ -233,29 +246,48 @@ __device__ void run_producer(const DecodeParams& p, uint32_t sbase, volatile int
 // ------------------------------------------------------------------------------------
 // MMA warp (one thread issues)
 // ------------------------------------------------------------------------------------
+// Warp-uniform wait: every lane polls, the warp leaves together (lane 0 decides timeouts).
+__device__ __forceinline__ bool warp_poll(uint32_t bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, mbar_try_wait(bar, parity) != 0);
+}
+__device__ __forceinline__ void mma_wait(const DecodeParams& p, uint32_t bar, uint32_t parity,
+                                         volatile int* abort_flag) {
+    if (warp_poll(bar, parity)) return;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        mbar_try_wait_hint(bar, parity, kPollHintNs);
+        if (warp_poll(bar, parity)) return;
+        const bool give_up = __shfl_sync(0xffffffffu, (*abort_flag != 0) || globaltimer_ns() - t0 > kWaitLimitNs, 0);
+        if (give_up) {
+            fail(p, abort_flag, kStatusTimeout);
+            return;
+        }
+    }
+}
+
+// The whole MMA warp runs this loop converged; the elected lane issues.
 __device__ void run_mma(const DecodeParams& p, uint32_t sbase, uint32_t tmem, volatile int* abort_flag, int nseg) {
     const Ring ring(p.kv_same);
     const uint32_t idq = idesc_e4m3(128, kTileTokens, false, false);
     const uint32_t idp = idesc_e4m3(128, kHeadsPerCta, true, false);
+    const uint32_t el = elect_one();
     auto barp = [&](int b) { return sbase + kOffBars + 8 * b; };
-    uint32_t tau = 0;
-    int qseg = 0;
+    int qseg = 0;  // non-empty units entered so far
 
     // Descriptors are formed once per tile and stepped by immediate offsets (the start
-    // address field counts 16-byte units), keeping the issue loop short: the issuing
-    // thread shares its scheduler with two softmax warps, and a slow issue would leave
-    // the tensor core idle.
-    const uint64_t pdesc = smem_desc(sbase + kOffP, 1024, 128, kSwizzleNone);
+    // address field counts 16-byte units).
+    const uint64_t pdesc0 = smem_desc(sbase + kOffP, 1024, 128, kSwizzleNone);
     auto issue_pv = [&](uint32_t tp, bool first) {
-        if (!mbar_wait(barp(BAR_PFULL), tp & 1, abort_flag)) fail(p, abort_flag, kStatusTimeout);
-        if (first && qseg > 0 && !mbar_wait(barp(BAR_OEMPTY), (qseg - 1) & 1, abort_flag))
-            fail(p, abort_flag, kStatusTimeout);
+        const int pb = tp & 1;
+        mma_wait(p, barp(BAR_PFULL0 + pb), (tp >> 1) & 1, abort_flag);
+        if (first && qseg > 0) mma_wait(p, barp(BAR_OEMPTY), (qseg - 1) & 1, abort_flag);
         tc_fence_after();
         const int e = static_cast<int>(tp % ring.slots);
         const uint32_t vbase = sbase + kOffRing + e * ring.slot_bytes + (p.kv_same ? 0u : kKvTileBytes);
         // V^T: 128 dims of block mc x 32 tokens (4 swizzle groups), MN-major. P'^T: 64 heads
         // x 32 tokens, K-major core matrices (token chunk stride 1 KB, head group 128 B).
         const uint64_t vdesc = smem_desc(vbase, 1024, kGroupBytes, kSwizzle128B);
+        const uint64_t pdesc = pdesc0 + static_cast<uint64_t>((pb * 2 * kPTermBytes) >> 4);
 #pragma unroll
         for (int mc = 0; mc < 4; ++mc) {
 #pragma unroll
@@ -265,14 +297,14 @@ __device__ void run_mma(const DecodeParams& p, uint32_t sbase, uint32_t tmem, vo
                 const uint64_t bl = pdesc + static_cast<uint64_t>((kPTermBytes + ks * 2048) >> 4);
                 const uint32_t d = tmem + kTmemO + mc * 64;
                 if (ks == 0)
-                    mma_e4m3(d, a, bh, idp, first ? 0u : 1u);
+                    mma_e4m3_el(d, a, bh, idp, first ? 0u : 1u, el);
                 else
-                    mma_e4m3_acc(d, a, bh, idp);
-                mma_e4m3_acc(d, a, bl, idp);
+                    mma_e4m3_acc_el(d, a, bh, idp, el);
+                mma_e4m3_acc_el(d, a, bl, idp, el);
             }
         }
-        tc_commit(barp(BAR_PVDONE));
-        tc_commit(barp(BAR_EMPTY0 + e));
+        tc_commit_el(barp(BAR_PVDONE0 + pb), el);
+        tc_commit_el(barp(BAR_EMPTY0 + e), el);
     };
 
     auto issue_qk = [&](uint32_t tq) {
@@ -281,26 +313,28 @@ __device__ void run_mma(const DecodeParams& p, uint32_t sbase, uint32_t tmem, vo
         tc_fence_after();
         // K: 128 tokens x 32 dims of block ks/4, K-major (8-token group stride 4 KB).
         const uint64_t kdesc = smem_desc(sbase + kOffRing + e * ring.slot_bytes, 16, kGroupBytes, kSwizzle128B);
-        const uint32_t d = tmem + kTmemS;
-        mma_e4m3_ta(d, tmem + kTmemQ, kdesc, idq, 0u);
+        const int sb = static_cast<int>(tq % kSBufs);
+        const uint32_t d = tmem + kTmemS + sb * kTileTokens;
+        mma_e4m3_ta_el(d, tmem + kTmemQ, kdesc, idq, 0u, el);
 #pragma unroll
         for (int ks = 1; ks < 16; ++ks)
-            mma_e4m3_ta_acc(d, tmem + kTmemQ + ks * 8, kdesc + static_cast<uint64_t>(((ks >> 2) * 1024 + (ks & 3) * 32) >> 4),
-                            idq);
-        tc_commit(barp(BAR_SFULL));
+            mma_e4m3_ta_acc_el(d, tmem + kTmemQ + ks * 8,
+                               kdesc + static_cast<uint64_t>(((ks >> 2) * 1024 + (ks & 3) * 32) >> 4), idq, el);
+        tc_commit_el(barp(BAR_SFULL0 + sb), el);
     };
-    // QK of tile tq may start once its ring slot is full and S has been read.
+    // QK of tile tq may start once its ring slot is full and its S buffer has been read.
     auto qk_ready = [&](uint32_t tq) {
         const int e = static_cast<int>(tq % ring.slots);
-        const bool full = mbar_try_wait(barp(BAR_FULL0 + e), (tq / ring.slots) & 1);
-        return full && (tq == 0 || mbar_try_wait(barp(BAR_SEMPTY), (tq - 1) & 1));
+        return warp_poll(barp(BAR_FULL0 + e), (tq / ring.slots) & 1) &&
+               (tq < kSBufs || warp_poll(barp(BAR_SEMPTY0 + static_cast<int>(tq % kSBufs)), ((tq / kSBufs) - 1) & 1));
     };
 
+    uint32_t tau = 0;
     for (int i = 0; i < nseg; ++i) {
         const Segment s = cta_segment(p.part, blockIdx.x, i);
         const Tiles tl = segment_tokens(p, s);
         if (tl.n <= 0) continue;
-        if (!mbar_wait(barp(BAR_QFULL), qseg & 1, abort_flag)) fail(p, abort_flag, kStatusTimeout);
+        mma_wait(p, barp(BAR_QFULL), qseg & 1, abort_flag);
         tc_fence_after();
         const uint32_t tau0 = tau;
         // QK(t) and PV(t-1) are independent: issue whichever becomes ready first.
@@ -311,23 +345,24 @@ __device__ void run_mma(const DecodeParams& p, uint32_t sbase, uint32_t tmem, vo
                 if (!qk_done && qk_ready(tau)) {
                     if (tau < 8) DSA_TRACE_AT(p, 56 + tau);
                     issue_qk(tau);
-                    if (t == tl.ntiles - 1) tc_commit(barp(BAR_QEMPTY));
+                    if (t == tl.ntiles - 1) tc_commit_el(barp(BAR_QEMPTY), el);
                     qk_done = true;
                 }
-                if (!pv_done && mbar_try_wait(barp(BAR_PFULL), (tau - 1) & 1)) {
+                if (!pv_done && warp_poll(barp(BAR_PFULL0 + ((tau - 1) & 1)), ((tau - 1) >> 1) & 1)) {
                     if (tau - 1 < 8) DSA_TRACE_AT(p, 64 + tau - 1);
                     issue_pv(tau - 1, tau - 1 == tau0);
                     pv_done = true;
                 }
                 if (!qk_done || !pv_done) {
-                    if (*abort_flag || globaltimer_ns() - t_start > kWaitLimitNs) {
+                    const bool give_up =
+                        __shfl_sync(0xffffffffu, (*abort_flag != 0) || globaltimer_ns() - t_start > kWaitLimitNs, 0);
+                    if (give_up) {
                         fail(p, abort_flag, kStatusTimeout);
                         break;
                     }
-                    // Sleep briefly on the barrier still awaited instead of spinning (the
-                    // spin would compete with the gather's copies for the memory pipe).
+                    // Sleep briefly on the barrier still awaited instead of spinning.
                     if (!pv_done)
-                        mbar_try_wait_hint(barp(BAR_PFULL), (tau - 1) & 1, kPollHintNs);
+                        mbar_try_wait_hint(barp(BAR_PFULL0 + ((tau - 1) & 1)), ((tau - 1) >> 1) & 1, kPollHintNs);
                     else
                         mbar_try_wait_hint(barp(BAR_FULL0 + static_cast<int>(tau % ring.slots)),
                                            (tau / ring.slots) & 1, kPollHintNs);
@@ -381,7 +416,7 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int sw = warp - kSoftmaxWarp0;      // 0..7
     const int q4 = warp & 3;                  // TMEM lane quarter of this warp
-    const int half = sw >> 2;                 // token half of each tile: columns [64*half, 64*half + 64)
+    const int half = sw >> 2;                 // token half of each tile: kHalfCols columns
     const int term = lane & 1;                // 0: hi row, 1: lo row
     const int hq = 16 * q4 + (lane >> 1);     // head of this thread within the unit
     const int st = sw * 32 + lane;            // 0..255
@@ -393,12 +428,34 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
     auto barp = [&](int b) { return sbase + kOffBars + 8 * b; };
     const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
     // This thread's first 16-byte row in a P' term buffer: K-major core matrices of 8 heads
-    // x 16 tokens, token chunk kc = 4*half + 2*term (+1 for the second), head group hq/8
-    // (chunk stride 1 KB, group stride 128 B).
-    const uint32_t p_off = ((4 * half + 2 * term) * 8 + (hq >> 3)) * 128 + (hq & 7) * 16;
+    // x 16 tokens, token chunk kc = (half*kHalfCols + term*kScores)/16 (+1 per further 16
+    // tokens), head group hq/8 (chunk stride 1 KB, group stride 128 B).
+    const uint32_t p_off = (((half * kHalfCols + term * kScores) / 16) * 8 + (hq >> 3)) * 128 + (hq & 7) * 16;
     uint32_t tau = 0;
     int qseg = 0;
 
+    // Query operand of a unit into TMEM (the previous unit's QKs must be done).
+    auto load_q = [&](int32_t unit) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.qimg + static_cast<int64_t>(unit) * kQImageBytes +
+                                                          (q4 * 32 + lane) * kLatent + half * 256);
+#pragma unroll
+        for (int hc = 0; hc < 2; ++hc) {
+            uint32_t a[32];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint4 v = src[hc * 8 + c];
+                a[4 * c] = v.x;
+                a[4 * c + 1] = v.y;
+                a[4 * c + 2] = v.z;
+                a[4 * c + 3] = v.w;
+            }
+            tmem_st_x32(tmem + lane_base + kTmemQ + half * 64 + hc * 32, a);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(barp(BAR_QFULL));
+    };
     for (int i = 0; i < nseg; ++i) {
         const Segment s = cta_segment(p.part, blockIdx.x, i);
         const Tiles tl = segment_tokens(p, s);
@@ -416,56 +473,38 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
             }
             continue;
         }
-
-        // ---- query operand of this unit into TMEM (after the previous unit's last QK) ----
+        // Query operand of this unit into TMEM, once the previous unit's QKs are done.
         if (qseg > 0) warp_wait(p, barp(BAR_QEMPTY), (qseg - 1) & 1, abort_flag);
-        {
-            const uint4* src = reinterpret_cast<const uint4*>(
-                p.qimg + static_cast<int64_t>(s.unit) * kQImageBytes + (q4 * 32 + lane) * kLatent + half * 256);
-#pragma unroll
-            for (int hc = 0; hc < 2; ++hc) {
-                uint32_t a[32];
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint4 v = src[hc * 8 + c];
-                    a[4 * c] = v.x;
-                    a[4 * c + 1] = v.y;
-                    a[4 * c + 2] = v.z;
-                    a[4 * c + 3] = v.w;
-                }
-                tmem_st_x32(tmem + lane_base + kTmemQ + half * 64 + hc * 32, a);
-            }
-            tmem_wait_st();
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(barp(BAR_QFULL));
+        load_q(s.unit);
         const float c = p.qscale[static_cast<int64_t>(s.unit) * kHeadsPerCta + hq];
         float m_ref = kNegInf;  // reference max of head hq (log2 units)
         float l_part = 0.0f;    // this thread's share of the row sum of P'
 
         for (int t = 0; t < tl.ntiles; ++t, ++tau) {
-            warp_wait(p, barp(BAR_SFULL), tau & 1, abort_flag);
+            const int sb = static_cast<int>(tau % kSBufs);
+            warp_wait(p, barp(BAR_SFULL0 + sb), (tau / kSBufs) & 1, abort_flag);
             if (st == 0 && tau < 8) DSA_TRACE_AT(p, 24 + tau);
             tc_fence_after();
-            uint32_t va[32], vb[32];
-            tmem_ld_x32(tmem + lane_base + kTmemS + half * 64, va);
-            tmem_ld_x32(tmem + lane_base + kTmemS + half * 64 + 32, vb);
+            uint32_t v[kHalfCols];
+#pragma unroll
+            for (int k = 0; k < kHalfCols / 32; ++k)
+                tmem_ld_x32(tmem + lane_base + kTmemS + sb * kTileTokens + half * kHalfCols + 32 * k,
+                            *reinterpret_cast<uint32_t(*)[32]>(v + 32 * k));
             if (st == 0 && (tau == 2 || tau == 3)) DSA_TRACE_AT(p, 72 + 8 * (tau - 2));
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(barp(BAR_SEMPTY));
+            if (lane == 0) mbar_arrive(barp(BAR_SEMPTY0 + sb));
 
-            // Scores of head hq for tokens tok0 .. tok0+31: this lane's term plus the
-            // neighbouring lane's other term. The hi lane keeps the first 32 columns of its
-            // half, the lo lane the last 32.
-            const int tok0 = t * kTileTokens + half * 64 + term * 32;
-            float x[32];
+            // Scores of head hq for tokens tok0 .. tok0+kScores-1: this lane's term plus the
+            // neighbouring lane's other term. The hi lane keeps the first kScores columns of
+            // its half, the lo lane the last kScores.
+            const int tok0 = t * kTileTokens + half * kHalfCols + term * kScores;
+            float x[kScores];
             bool over = false;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const float send = __uint_as_float(term ? va[j] : vb[j]);
-                const float mine = __uint_as_float(term ? vb[j] : va[j]);
+            for (int j = 0; j < kScores; ++j) {
+                const float send = __uint_as_float(term ? v[j] : v[kScores + j]);
+                const float mine = __uint_as_float(term ? v[kScores + j] : v[j]);
                 const float other = __shfl_xor_sync(0xffffffffu, send, 1);
                 x[j] = (tok0 + j < tl.n) ? (mine + other) * c : kNegInf;
                 over |= x[j] > m_ref + kRescaleMargin;
@@ -477,7 +516,7 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
                 // than the margin; rescale O and the row sums by 2^(m_old - m_new).
                 float hmax = x[0];
 #pragma unroll
-                for (int j = 1; j < 32; ++j) hmax = fmaxf(hmax, x[j]);
+                for (int j = 1; j < kScores; ++j) hmax = fmaxf(hmax, x[j]);
                 hmax = fmaxf(hmax, __shfl_xor_sync(0xffffffffu, hmax, 1));
                 if (term == 0) hm_s[half * kHeadsPerCta + hq] = hmax;
                 named_bar_sync<kBarSoftmax, kSoftmaxThreads>();
@@ -490,21 +529,28 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
                 if (term == 0 && half == 0) alpha_s[hq] = alpha;
                 named_bar_sync<kBarSoftmax, kSoftmaxThreads>();
                 if (t > 0) {
-                    float amin = 1.0f;
+                    // Blocks of 32 heads whose factors are all 1 are left alone.
+                    float bmin[2];
 #pragma unroll
-                    for (int h = 0; h < kHeadsPerCta; h += 4) {
-                        const float4 a4 = *reinterpret_cast<const float4*>(alpha_s + h);
-                        amin = fminf(amin, fminf(fminf(a4.x, a4.y), fminf(a4.z, a4.w)));
+                    for (int hh = 0; hh < 2; ++hh) {
+                        float m = 1.0f;
+#pragma unroll
+                        for (int h = 0; h < 32; h += 4) {
+                            const float4 a4 = *reinterpret_cast<const float4*>(alpha_s + hh * 32 + h);
+                            m = fminf(m, fminf(fminf(a4.x, a4.y), fminf(a4.z, a4.w)));
+                        }
+                        bmin[hh] = m;
                     }
-                    if (amin < 1.0f) {
+                    if (fminf(bmin[0], bmin[1]) < 1.0f) {
                         // O^T columns are heads: this warp rescales its lanes of chunks
                         // 2*half and 2*half + 1, once the P.V before this tile is done.
-                        warp_wait(p, barp(BAR_PVDONE), (tau - 1) & 1, abort_flag);
+                        warp_wait(p, barp(BAR_PVDONE0 + ((tau - 1) & 1)), ((tau - 1) >> 1) & 1, abort_flag);
                         tc_fence_after();
 #pragma unroll 1
                         for (int mc2 = 0; mc2 < 2; ++mc2) {
 #pragma unroll 1
                             for (int hh = 0; hh < 2; ++hh) {
+                                if (bmin[hh] >= 1.0f) continue;
                                 const uint32_t ta = tmem + lane_base + kTmemO + (2 * half + mc2) * 64 + hh * 32;
                                 uint32_t o[32];
                                 tmem_ld_x32(ta, o);
@@ -520,10 +566,10 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
             }
 
             // P' = 2^(x - m + kPBias) as two E4M3 terms, 16 tokens per 16-byte row.
-            uint32_t hw[8], lw[8];
+            uint32_t hw[kScores / 4], lw[kScores / 4];
             float lsum = 0.0f;
 #pragma unroll
-            for (int g = 0; g < 8; ++g) {
+            for (int g = 0; g < kScores / 4; ++g) {
                 float ph[4], pl[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -537,24 +583,25 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
             }
             l_part += lsum;
             if (st == 0 && (tau == 2 || tau == 3)) DSA_TRACE_AT(p, 74 + 8 * (tau - 2));
-            // The P buffer is free once the previous tile's P.V has finished reading it.
-            if (tau >= 1) warp_wait(p, barp(BAR_PVDONE), (tau - 1) & 1, abort_flag);
+            // P buffer tau%2 is free once the P.V two tiles back has finished reading it.
+            if (tau >= 2) warp_wait(p, barp(BAR_PVDONE0 + (tau & 1)), ((tau >> 1) - 1) & 1, abort_flag);
             if (st == 0 && (tau == 2 || tau == 3)) DSA_TRACE_AT(p, 75 + 8 * (tau - 2));
-            const uint32_t pb = sbase + kOffP;
-            st_shared_v4(pb + p_off, hw[0], hw[1], hw[2], hw[3]);
-            st_shared_v4(pb + p_off + 1024, hw[4], hw[5], hw[6], hw[7]);
-            st_shared_v4(pb + kPTermBytes + p_off, lw[0], lw[1], lw[2], lw[3]);
-            st_shared_v4(pb + kPTermBytes + p_off + 1024, lw[4], lw[5], lw[6], lw[7]);
+            const uint32_t pb = sbase + kOffP + (tau & 1) * 2 * kPTermBytes;
+#pragma unroll
+            for (int c = 0; c < kScores / 16; ++c) {
+                st_shared_v4(pb + p_off + c * 1024, hw[4 * c], hw[4 * c + 1], hw[4 * c + 2], hw[4 * c + 3]);
+                st_shared_v4(pb + kPTermBytes + p_off + c * 1024, lw[4 * c], lw[4 * c + 1], lw[4 * c + 2], lw[4 * c + 3]);
+            }
             fence_proxy_async_smem();
             if (st == 0 && (tau == 2 || tau == 3)) DSA_TRACE_AT(p, 76 + 8 * (tau - 2));
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(barp(BAR_PFULL));
+            if (lane == 0) mbar_arrive(barp(BAR_PFULL0 + (tau & 1)));
             if (st == 0 && tau < 8) DSA_TRACE_AT(p, 32 + tau);
         }
 
         // ---- epilogue ----
-        warp_wait(p, barp(BAR_PVDONE), (tau - 1) & 1, abort_flag);
+        warp_wait(p, barp(BAR_PVDONE0 + ((tau - 1) & 1)), ((tau - 1) >> 1) & 1, abort_flag);
         if (st == 0 && i == 0) DSA_TRACE_AT(p, 17);
         tc_fence_after();
         const float lpair = l_part + __shfl_xor_sync(0xffffffffu, l_part, 1);
@@ -614,15 +661,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
 
     if (tid == 0) {
         const uint32_t b = sbase + kOffBars;
-        for (int e = 0; e < 3; ++e) {
-            // one cp.async arrival and one plain arrival per lane of each quarter
-            mbar_init(b + 8 * (BAR_FULL0 + e), 2 * 32 * kQuarters);
+        for (int e = 0; e < kSlotsKV; ++e) {
+            // one copy-completion arrival per gather lane
+            mbar_init(b + 8 * (BAR_FULL0 + e), 32 * kProducerWarps);
             mbar_init(b + 8 * (BAR_EMPTY0 + e), 1);
         }
-        mbar_init(b + 8 * BAR_SFULL, 1);
-        mbar_init(b + 8 * BAR_SEMPTY, kSoftmaxWarps);
-        mbar_init(b + 8 * BAR_PFULL, kSoftmaxWarps);
-        mbar_init(b + 8 * BAR_PVDONE, 1);
+        for (int k = 0; k < kSBufs; ++k) {
+            mbar_init(b + 8 * (BAR_SFULL0 + k), 1);
+            mbar_init(b + 8 * (BAR_SEMPTY0 + k), kSoftmaxWarps);
+        }
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(b + 8 * (BAR_PFULL0 + k), kSoftmaxWarps);
+            mbar_init(b + 8 * (BAR_PVDONE0 + k), 1);
+        }
         mbar_init(b + 8 * BAR_QFULL, kSoftmaxWarps);
         mbar_init(b + 8 * BAR_QEMPTY, 1);
         mbar_init(b + 8 * BAR_OEMPTY, kSoftmaxWarps);
@@ -649,20 +700,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     if (warp < kProducerWarps) {
         run_producer(p, sbase, abort_flag, nseg);
     } else if (warp == kMmaWarp) {
-        if (lane == 0) {
-            run_mma(p, sbase, tmem, abort_flag, nseg);
-            // Wait (bounded, regardless of abort) until every issued MMA has completed and
-            // the softmax warps have finished reading TMEM.
-            const uint32_t db = sbase + kOffBars + 8 * BAR_DRAIN;
-            tc_commit(db);
-            uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(db, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
-            }
-            DSA_TRACE_AT(p, 11);
-            const uint32_t done = sbase + kOffBars + 8 * BAR_DONE;
-            t0 = globaltimer_ns();
-            while (!mbar_try_wait(done, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
-            }
+        run_mma(p, sbase, tmem, abort_flag, nseg);
+        // Wait (bounded, regardless of abort) until every issued MMA has completed and the
+        // softmax warps have finished reading TMEM.
+        const uint32_t db = sbase + kOffBars + 8 * BAR_DRAIN;
+        tc_commit_el(db, elect_one());
+        uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(db, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+        }
+        DSA_TRACE_AT(p, 11);
+        const uint32_t done = sbase + kOffBars + 8 * BAR_DONE;
+        t0 = globaltimer_ns();
+        while (!mbar_try_wait(done, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
         }
         __syncwarp();
     } else {
