@@ -14,7 +14,9 @@
 namespace dsa {
 namespace {
 
-constexpr int kCombineThreads = 128;  // 4 latent dims per thread; also pieces per chunk
+constexpr int kCombineThreads = 256;
+constexpr int kCombineHeads = kCombineThreads / 64;  // heads per block; 64 threads x 8 dims per head
+constexpr int kPieceBatch = 8;                        // partial loads in flight per thread
 constexpr float kNegInfC = -__builtin_huge_valf();
 
 // Partial slot of unit u in CTA c, or -1 when CTA c has no slots at all.
@@ -24,93 +26,88 @@ __device__ __forceinline__ int32_t piece_slot(const Partition& part, int64_t u, 
     return static_cast<int32_t>(2 * c + (u == b / part.width ? 0 : 1));
 }
 
-__device__ __forceinline__ float block_max(float v, float* red) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    const float m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-    __syncthreads();
-    return m;
-}
-
+// Block (u, hb): heads hb*4 .. hb*4+3 of unit u; thread t: head hb*4 + t/64, dims 8*(t%64) ..
+// +8. The block first finds the pieces' partial slots and the four heads' lse values (one
+// piece per thread, up to 256 pieces per round, into shared memory); then every thread folds
+// the pieces' 16-byte slices of its head into a running softmax, kPieceBatch loads at a time.
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams p) {
     // Launched as a programmatic dependent of the decode kernel: wait for its partials.
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    __shared__ int32_t slot_s[kCombineThreads];
+    __shared__ float lse_s[kCombineHeads][kCombineThreads];
     const int64_t u = blockIdx.x;
-    const int hl = blockIdx.y;
+    const int hh = threadIdx.x >> 6;
+    const int hl = blockIdx.y * kCombineHeads + hh;
+    const int dim0 = (threadIdx.x & 63) * 8;
     const int32_t r = static_cast<int32_t>(u / p.part.groups), g = static_cast<int32_t>(u % p.part.groups);
     const int32_t h = g * kHeadsPerCta + hl;
-    if (h >= p.heads) return;
     const int64_t W = p.part.width;
     const int64_t c_lo = cta_of_slot(p.part, u * W);
     const int64_t c_hi = cta_of_slot(p.part, (u + 1) * W - 1);
-    if (c_lo == c_hi) return;
+    if (c_lo == c_hi) return;  // written whole by the decode kernel (uniform over the block)
 
-    __shared__ float red[4];
-    __shared__ float w_s[kCombineThreads];
-    __shared__ int32_t slot_s[kCombineThreads];
-    // Pass 1: the largest log-sum-exp over the pieces.
-    float mx = kNegInfC;
+    float mx = kNegInfC, wsum = 0.0f;
+    float acc[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[k] = 0.0f;
     for (int64_t c0 = c_lo; c0 <= c_hi; c0 += kCombineThreads) {
-        const int64_t c = c0 + threadIdx.x;
-        float lse = kNegInfC;
-        if (c <= c_hi) {
-            const int32_t slot = piece_slot(p.part, u, c);
-            if (slot >= 0) lse = p.part_lse[static_cast<int64_t>(slot) * kHeadsPerCta + hl];
+        const int n = static_cast<int>(min(c_hi + 1 - c0, static_cast<int64_t>(kCombineThreads)));
+        __syncthreads();  // the previous round's smem is no longer read
+        if (static_cast<int>(threadIdx.x) < n) {
+            const int32_t slot = piece_slot(p.part, u, c0 + threadIdx.x);
+            slot_s[threadIdx.x] = slot;
+#pragma unroll
+            for (int k = 0; k < kCombineHeads; ++k)
+                lse_s[k][threadIdx.x] =
+                    slot >= 0 ? p.part_lse[static_cast<int64_t>(slot) * kHeadsPerCta + blockIdx.y * kCombineHeads + k]
+                              : kNegInfC;
         }
-        mx = fmaxf(mx, block_max(lse, red));
-    }
-    // Pass 2: out = v_scale * sum_k 2^(lse_k - mx) O_k / sum_k 2^(lse_k - mx).
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float wsum = 0.0f;
-    if (mx != kNegInfC) {
-        for (int64_t c0 = c_lo; c0 <= c_hi; c0 += kCombineThreads) {
-            const int n = static_cast<int>(min(c_hi + 1 - c0, static_cast<int64_t>(kCombineThreads)));
-            if (threadIdx.x < n) {
-                const int32_t slot = piece_slot(p.part, u, c0 + threadIdx.x);
-                float w = 0.0f;
-                if (slot >= 0) w = exp2f(p.part_lse[static_cast<int64_t>(slot) * kHeadsPerCta + hl] - mx);
-                slot_s[threadIdx.x] = slot;
-                w_s[threadIdx.x] = w;
+        __syncthreads();
+        float m = mx;
+        for (int e = 0; e < n; ++e) m = fmaxf(m, lse_s[hh][e]);
+        if (m == kNegInfC) continue;
+        if (m > mx) {  // rescale what was folded so far
+            const float a = mx == kNegInfC ? 0.0f : exp2f(mx - m);
+            wsum *= a;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) acc[k] *= a;
+            mx = m;
+        }
+        for (int e0 = 0; e0 < n; e0 += kPieceBatch) {
+            uint4 raw[kPieceBatch];
+            float w[kPieceBatch];
+#pragma unroll
+            for (int e = 0; e < kPieceBatch; ++e) {
+                const int k = e0 + e;
+                w[e] = k < n ? exp2f(lse_s[hh][k] - mx) : 0.0f;
+                raw[e] = make_uint4(0, 0, 0, 0);
+                if (w[e] != 0.0f)
+                    raw[e] = *reinterpret_cast<const uint4*>(
+                        p.part_o + (static_cast<int64_t>(slot_s[k]) * kHeadsPerCta + hl) * kLatent + dim0);
             }
-            __syncthreads();
-            for (int k0 = 0; k0 < n; k0 += 8) {
-                float4 o[8];
-                float w[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int k = k0 + e;
-                    w[e] = k < n ? w_s[k] : 0.0f;
-                    if (w[e] != 0.0f) {
-                        const uint2 raw = reinterpret_cast<const uint2*>(
-                            p.part_o + (static_cast<int64_t>(slot_s[k]) * kHeadsPerCta + hl) * kLatent)[threadIdx.x];
-                        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
-                        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
-                        o[e] = make_float4(a.x, a.y, b.x, b.y);
-                    } else {
-                        o[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-                }
+            for (int e = 0; e < kPieceBatch; ++e) {
+                wsum += w[e];
+                const __half2* hv = reinterpret_cast<const __half2*>(&raw[e]);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    wsum += w[e];
-                    acc.x += w[e] * o[e].x;
-                    acc.y += w[e] * o[e].y;
-                    acc.z += w[e] * o[e].z;
-                    acc.w += w[e] * o[e].w;
+                for (int k = 0; k < 4; ++k) {
+                    const float2 f = __half22float2(hv[k]);
+                    acc[2 * k] += w[e] * f.x;
+                    acc[2 * k + 1] += w[e] * f.y;
                 }
             }
-            __syncthreads();
         }
     }
+    if (h >= p.heads) return;
     const float f = wsum > 0.0f ? p.v_scale / wsum : 0.0f;
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * f, acc.y * f);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * f, acc.w * f);
-    uint2 packed;
-    packed.x = *reinterpret_cast<uint32_t*>(&lo);
-    packed.y = *reinterpret_cast<uint32_t*>(&hi);
-    reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(r) * p.heads + h) * kLatent)[threadIdx.x] = packed;
+    uint4 packed;
+    uint32_t* pw = reinterpret_cast<uint32_t*>(&packed);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * k] * f, acc[2 * k + 1] * f);
+        pw[k] = *reinterpret_cast<uint32_t*>(&b);
+    }
+    *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(r) * p.heads + h) * kLatent + dim0) = packed;
 }
 
 }  // namespace
@@ -125,7 +122,7 @@ cudaError_t combine_kernel_setup() {
 cudaError_t launch_combine(const CombineParams& p, int units, cudaStream_t stream) {
     if (units <= 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(units, kHeadsPerCta);
+    cfg.gridDim = dim3(units, kHeadsPerCta / kCombineHeads);
     cfg.blockDim = dim3(kCombineThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;

@@ -178,9 +178,12 @@ __device__ void run_producer(const DecodeParams& p, uint32_t sbase, volatile int
     const int r0 = warp * kWarpRows;
     const int nr = min(kWarpRows, kTileTokens - r0);
     uint32_t tau = 0;
+    if (tid == 0) DSA_TRACE_AT(p, 2);
     for (int i = 0; i < nseg; ++i) {
         const Segment s = cta_segment(p.part, blockIdx.x, i);
+        if (tid == 0 && i == 0) DSA_TRACE_AT(p, 3);
         const Tiles tl = segment_tokens(p, s);
+        if (tid == 0 && i == 0 && tl.n >= 0) DSA_TRACE_AT(p, 4);
         if (tl.n <= 0) continue;
         const long long* offs = p.offs + static_cast<int64_t>(s.row) * W + tl.t0;
         // This lane's rows of tile t: r0 + lane and r0 + 32 + lane (the latter for lane < nr - 32).
@@ -193,10 +196,13 @@ __device__ void run_producer(const DecodeParams& p, uint32_t sbase, volatile int
         load(0, oa, ob);
         for (int t = 0; t < tl.ntiles; ++t, ++tau) {
             const long long ca = oa, cb = ob;
+            if (tid == 0 && t == 0 && i == 0 && ca != 12345) DSA_TRACE_AT(p, 5);
             load(t + 1, oa, ob);  // next tile's rows, before the slot wait
+            if (tid == 0 && t == 0 && i == 0) DSA_TRACE_AT(p, 6);
             if ((ca < 0 && t * kTileTokens + r0 + lane < tl.n) ||
                 (cb < 0 && lane + 32 < nr && t * kTileTokens + r0 + 32 + lane < tl.n))
                 atomicCAS(p.status, 0, kStatusBounds);
+            if (tid == 0 && t == 0 && i == 0) DSA_TRACE_AT(p, 7);
             const int e = static_cast<int>(tau % ring.slots);
             const uint32_t use = tau / ring.slots;
             if (tau >= static_cast<uint32_t>(ring.slots))
@@ -436,14 +442,16 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
 
     // Query operand of a unit into TMEM (the previous unit's QKs must be done).
     auto load_q = [&](int32_t unit) {
+        // Chunk-major image (chunk c of row r at c*2048 + r*16): each load of the warp is 512
+        // contiguous bytes.
         const uint4* src = reinterpret_cast<const uint4*>(p.qimg + static_cast<int64_t>(unit) * kQImageBytes +
-                                                          (q4 * 32 + lane) * kLatent + half * 256);
+                                                          half * 16 * 2048 + (q4 * 32 + lane) * 16);
 #pragma unroll
         for (int hc = 0; hc < 2; ++hc) {
             uint32_t a[32];
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                const uint4 v = src[hc * 8 + c];
+                const uint4 v = src[(hc * 8 + c) * (2048 / 16)];
                 a[4 * c] = v.x;
                 a[4 * c + 1] = v.y;
                 a[4 * c + 2] = v.z;

@@ -14,13 +14,18 @@
 // the operand image the decode kernel loads into tensor memory: per head a power-of-two
 // scale 2^e (|q|*2^e < 256) and two E4M3 terms hi + lo whose sum is q*2^e. hi keeps the
 // top 4 significant bits (truncation), lo is the remainder; for |q*2^e| >= 2^-2 the
-// split is exact, since a BF16 value has 8 significant bits. The image is 128 rows of
-// 512 codes; row 32q + 2k + t holds term t of head 16q + k.
+// split is exact, since a BF16 value has 8 significant bits. The image holds 128 rows of
+// 512 codes (row 32q + 2k + t = term t of head 16q + k), stored chunk-major: the 16 bytes
+// of chunk c of row r are at c*2048 + r*16.
 #include "common.cuh"
 #include "ptx.cuh"
 
 namespace dsa {
 namespace {
+
+constexpr int kMaxSel = DSA_MAX_SEL_WIDTH;                        // resolved ids per row, at most
+constexpr int kPrologueSmem = kBitmapWords * 4 + kMaxSel * 4;     // bitmap or keys, then the ids
+constexpr int kBatch = 8;                                         // loads in flight per thread
 
 __device__ __forceinline__ int32_t row_seq_len(const PrologueParams& p, int32_t r) {
     int32_t L = p.verify_rows ? p.seq_lens[r / p.rows_per_seq] + (r % p.rows_per_seq) + 1 : p.seq_lens[r];
@@ -66,7 +71,8 @@ __device__ __forceinline__ long long token_offset(const PrologueParams& p, int32
 }
 
 
-__device__ void resolve_row(const PrologueParams& p, int32_t r, uint32_t* sm, int32_t* scratch) {
+// sm: kBitmapWords words of scratch (bitmap or sort keys); ids_s: kMaxSel resolved ids.
+__device__ void resolve_row(const PrologueParams& p, int32_t r, uint32_t* sm, int32_t* ids_s, int32_t* scratch) {
     const int tid = threadIdx.x;
     const int32_t W = p.width;
     const int32_t L = row_seq_len(p, r);
@@ -77,11 +83,28 @@ __device__ void resolve_row(const PrologueParams& p, int32_t r, uint32_t* sm, in
     int32_t total = 0;
     if (L <= kBitmapWords * 32) {
         const int32_t nwords = (L + 31) >> 5;
+        // The first batch of the selection row is loaded while the bitmap is cleared.
+        int32_t idv[kBatch];
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const int32_t j = tid + k * kResolveThreads;
+            idv[k] = j < W ? sel[j] : -1;
+        }
         for (int32_t w = tid; w < nwords; w += kResolveThreads) sm[w] = 0u;
         __syncthreads();
-        for (int32_t j = tid; j < W; j += kResolveThreads) {
-            const int32_t id = sel[j];
-            if (id >= 0 && id < L) atomicOr(&sm[id >> 5], 1u << (id & 31));
+        for (int32_t j0 = tid;; j0 += kBatch * kResolveThreads) {
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const int32_t id = idv[k];
+                if (id >= 0 && id < L) atomicOr(&sm[id >> 5], 1u << (id & 31));
+            }
+            const int32_t n0 = j0 + kBatch * kResolveThreads;
+            if (n0 - tid >= W) break;
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const int32_t j = n0 + k * kResolveThreads;
+                idv[k] = j < W ? sel[j] : -1;
+            }
         }
         __syncthreads();
         const int32_t per = (nwords + kResolveThreads - 1) / kResolveThreads;
@@ -94,7 +117,7 @@ __device__ void resolve_row(const PrologueParams& p, int32_t r, uint32_t* sm, in
             uint32_t bits = sm[w];
             while (bits) {
                 const int b = __ffs(bits) - 1;
-                ids[pos++] = w * 32 + b;
+                ids_s[pos++] = w * 32 + b;
                 bits &= bits - 1;
             }
         }
@@ -131,25 +154,23 @@ __device__ void resolve_row(const PrologueParams& p, int32_t r, uint32_t* sm, in
             mine += (keys[j] != INT32_MAX && (j == 0 || keys[j] != keys[j - 1])) ? 1 : 0;
         int32_t pos = block_exclusive_scan(mine, scratch, &total);
         for (int32_t j = j0; j < j1; ++j)
-            if (keys[j] != INT32_MAX && (j == 0 || keys[j] != keys[j - 1])) ids[pos++] = keys[j];
+            if (keys[j] != INT32_MAX && (j == 0 || keys[j] != keys[j - 1])) ids_s[pos++] = keys[j];
     }
-    for (int32_t j = total + tid; j < W; j += kResolveThreads) ids[j] = -1;
+    __syncthreads();
+    // Coalesced write-out of the ids (-1 padded), then each id's byte offset with all of a
+    // thread's block-table loads in flight at once.
+    for (int32_t j = tid; j < W; j += kResolveThreads) ids[j] = j < total ? ids_s[j] : -1;
     if (tid == 0) p.cnt[r] = total;
     if (!offs) return;
-    // Byte offsets, four independent id and block-table loads in flight per thread.
-    __syncthreads();
-    for (int32_t j0 = tid; j0 < total; j0 += 4 * kResolveThreads) {
-        int32_t id[4];
+    for (int32_t j0 = tid; j0 < total; j0 += kBatch * kResolveThreads) {
+        long long o[kBatch];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
+        for (int e = 0; e < kBatch; ++e) {
             const int32_t j = j0 + e * kResolveThreads;
-            id[e] = j < total ? ids[j] : 0;
+            o[e] = j < total ? token_offset(p, seq, ids_s[j]) : 0;
         }
-        long long o[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) o[e] = token_offset(p, seq, id[e]);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
+        for (int e = 0; e < kBatch; ++e) {
             const int32_t j = j0 + e * kResolveThreads;
             if (j < total) offs[j] = o[e];
         }
@@ -213,11 +234,13 @@ __device__ void prepare_queries(const PrologueParams& p, int32_t unit) {
             hi[k] = f32x2_to_e4m3x2(vh[0], vh[1]) | (f32x2_to_e4m3x2(vh[2], vh[3]) << 16);
             lo[k] = f32x2_to_e4m3x2(vl[0], vl[1]) | (f32x2_to_e4m3x2(vl[2], vl[3]) << 16);
         }
-        // Row-major image: rows 2k and 2k+1 of quarter q hold the hi and lo terms of head
-        // 16q + k, so the decode finds both terms of a head in neighbouring TMEM lanes.
+        // Rows 2k and 2k+1 of quarter q hold the hi and lo terms of head 16q + k, so the
+        // decode finds both terms of a head in neighbouring TMEM lanes. The image is stored
+        // chunk-major ([32 chunks of 16 bytes][128 rows][16 bytes]): 32 consecutive rows of
+        // one chunk are 512 contiguous bytes, which the decode reads one row per lane.
         const int rh = 32 * (hl >> 4) + 2 * (hl & 15);
-        *reinterpret_cast<uint4*>(img + rh * kLatent + lane * 16) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(img + (rh + 1) * kLatent + lane * 16) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        *reinterpret_cast<uint4*>(img + lane * 2048 + rh * 16) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(img + lane * 2048 + (rh + 1) * 16) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         if (lane == 0)
             p.qscale[static_cast<int64_t>(unit) * kHeadsPerCta + hl] =
                 p.score_scale * __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
@@ -225,14 +248,14 @@ __device__ void prepare_queries(const PrologueParams& p, int32_t unit) {
 }
 
 __global__ void __launch_bounds__(kResolveThreads) prologue_kernel(const PrologueParams p) {
-    extern __shared__ __align__(16) uint32_t bitmap[];
+    extern __shared__ __align__(16) uint32_t bitmap[];  // kBitmapWords words, then kMaxSel ids
     __shared__ int32_t scratch[kResolveThreads / 32];
     // Let the decode kernel launch and run its set-up while this grid finishes; it waits
     // for this grid's completion before reading anything written here.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (blockIdx.x == 0 && threadIdx.x == 0 && p.status) atomicExch(p.status, 0);
     if (static_cast<int32_t>(blockIdx.x) < p.rows)
-        resolve_row(p, blockIdx.x, bitmap, scratch);
+        resolve_row(p, blockIdx.x, bitmap, reinterpret_cast<int32_t*>(bitmap + kBitmapWords), scratch);
     else
         prepare_queries(p, blockIdx.x - p.rows);
 }
@@ -243,6 +266,8 @@ cudaError_t prologue_kernel_setup() {
     cudaFuncAttributes attr;
     cudaError_t e = cudaFuncGetAttributes(&attr, prologue_kernel);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(prologue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrologueSmem);
+    if (e != cudaSuccess) return e;
     // Same shared-memory carveout as the decode kernel, so the SMs need no
     // reconfiguration between the two.
     return cudaFuncSetAttribute(prologue_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
@@ -250,7 +275,7 @@ cudaError_t prologue_kernel_setup() {
 
 cudaError_t launch_prologue(const PrologueParams& p, int blocks, cudaStream_t stream) {
     if (blocks <= 0) return cudaSuccess;
-    prologue_kernel<<<blocks, kResolveThreads, kBitmapWords * 4, stream>>>(p);
+    prologue_kernel<<<blocks, kResolveThreads, kPrologueSmem, stream>>>(p);
     return cudaGetLastError();
 }
 
