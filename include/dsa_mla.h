@@ -204,6 +204,19 @@ int32_t dsa_mla_decode_static(const void* q, const void* k_cache, const void* v_
                               float v_scale, float sm_scale, void* out, void* stream);
 
 /*
+ * dsa_set_tile_tokens: KV tokens per decode tile for every later call in this process.
+ *  tile_tokens  0 = automatic (the default): 64-token tiles when each decode CTA has at
+ *               most 256 selected slots of work (small batches, where a shorter pipeline
+ *               matters most), 128-token tiles otherwise (better tensor-core use);
+ *               64 or 128 = that size for every call.
+ * Results agree with either size to floating-point rounding order. Any other value
+ * returns DSA_ERR_INVALID_ARGUMENT and changes nothing. Calls already enqueued, or
+ * captured into a CUDA graph, keep the size they were launched with. Not thread-safe
+ * against concurrent decode calls. The source pages have no counterpart to this call.
+ */
+int32_t dsa_set_tile_tokens(int32_t tile_tokens);
+
+/*
  * Device status of the latest call on a caller workspace (dsa_mla_decode_ws /
  * dsa_mla_decode_host) or on the library workspace of the current device
  * (dsa_last_device_status). Synchronises the stream, writes the status to *status_out

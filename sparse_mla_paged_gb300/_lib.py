@@ -28,6 +28,7 @@ _P, _I32, _I64, _F32, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, cty
 _DECODE_ARGS = [_P, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I64, _F32, _F32, _F32, _P]
 SIGNATURES = {
     "dsa_abi_version": ([], _I32),
+    "dsa_set_tile_tokens": ([_I32], _I32),
     "dsa_status_string": ([_I32], ctypes.c_char_p),
     "dsa_mla_decode": (_DECODE_ARGS + [_P], _I32),
     "dsa_mla_decode_k": (_DECODE_ARGS + [_P], _I32),

@@ -35,6 +35,11 @@ def abi_version() -> int:
     return int(_lib.load().dsa_abi_version())
 
 
+def set_tile_tokens(tile_tokens: int) -> None:
+    """KV tokens per decode tile for later calls: 0 = automatic, 64 or 128 (dsa_set_tile_tokens)."""
+    _lib.check(_lib.load().dsa_set_tile_tokens(int(tile_tokens)), "dsa_set_tile_tokens")
+
+
 def status_string(status: int) -> str:
     return _lib.load().dsa_status_string(int(status)).decode()
 

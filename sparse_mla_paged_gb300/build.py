@@ -17,6 +17,10 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdsa_mla.so")
 SOURCES = ["api.cu", "prologue.cu", "decode.cu", "combine.cu", "static_scratch.cu"]
+# Translation units: (source, object, extra flags); decode.cu is built once per tile size.
+UNITS = [("api.cu", "api.o", []), ("prologue.cu", "prologue.o", []),
+         ("decode.cu", "decode64.o", ["-DDSA_TILE=64"]), ("decode.cu", "decode128.o", ["-DDSA_TILE=128"]),
+         ("combine.cu", "combine.o", []), ("static_scratch.cu", "static_scratch.o", [])]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -31,10 +35,11 @@ def nvcc() -> str:
     return p
 
 
-def _compile(src: str, extra: list[str]) -> str:
-    obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+def _compile(unit, extra: list[str]) -> str:
+    src, obj_name, flags = unit
+    obj = os.path.join(BUILD, obj_name)
     cmd = [nvcc(), *ARCH, "-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
-           "-I", CSRC, "-c", os.path.join(CSRC, src), "-o", obj, *extra]
+           "-I", CSRC, *flags, "-c", os.path.join(CSRC, src), "-o", obj, *extra]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
@@ -55,8 +60,8 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
-    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), SOURCES))
+    with cf.ThreadPoolExecutor(max_workers=len(UNITS)) as ex:
+        objs = list(ex.map(lambda u: _compile(u, extra), UNITS))
     tmp = LIB + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)

@@ -22,6 +22,7 @@ struct DeviceState {
 
 std::mutex g_mu;
 std::vector<DeviceState> g_devices;
+int32_t g_tile_tokens = 0;  // dsa_set_tile_tokens: 0 = automatic, else 64 or 128
 #ifdef DSA_TRACE
 unsigned long long* g_trace = nullptr;  // trace builds only: per-CTA decode timeline
 #endif
@@ -86,7 +87,8 @@ int32_t current_device(DeviceState** out) {
         if (major != 10 || minor != 3) {
             d.status = DSA_ERR_UNSUPPORTED;
         } else {
-            d.status = from_cuda(decode_kernel_setup());
+            d.status = from_cuda(decode_kernel_setup_64());
+            if (d.status == DSA_OK) d.status = from_cuda(decode_kernel_setup_128());
             if (d.status == DSA_OK) d.status = from_cuda(prologue_kernel_setup());
             if (d.status == DSA_OK) d.status = from_cuda(combine_kernel_setup());
         }
@@ -100,6 +102,7 @@ struct Plan {
     int64_t rows, groups, units;
     Partition part;
     bool any_split;
+    bool small_tiles;  // 64-token tiles: at most two 128-slot tiles of work per CTA
     WsLayout ws;
 };
 
@@ -118,6 +121,7 @@ Plan make_plan(int64_t rows, int32_t heads, int32_t width, int32_t num_ctas, int
         if (c < 1) c = 1;
     }
     pl.part.ctas = static_cast<int32_t>(c);
+    pl.small_tiles = g_tile_tokens == 0 ? pl.part.total_slots <= 2 * kCtaMinSlots * c : g_tile_tokens == 64;
     pl.any_split = false;
     for (int64_t k = 1; k < c && !pl.any_split; ++k)
         if (cta_begin(pl.part, k) % width != 0) pl.any_split = true;
@@ -181,7 +185,7 @@ int32_t enqueue(const Args& a, const Plan& pl, uint8_t* ws, cudaEvent_t ev0, cud
         if (cs == cudaStreamCaptureStatusActive) ev_flags = cudaEventRecordExternal;
     }
     if (ev0 && cudaEventRecordWithFlags(ev0, stream, ev_flags) != cudaSuccess) return DSA_ERR_CUDA;
-    st = from_cuda(launch_decode(dp, stream));
+    st = from_cuda(pl.small_tiles ? launch_decode_64(dp, stream) : launch_decode_128(dp, stream));
     if (st != DSA_OK) return st;
     if (ev1 && cudaEventRecordWithFlags(ev1, stream, ev_flags) != cudaSuccess) return DSA_ERR_CUDA;
 
@@ -276,6 +280,12 @@ void dsa_debug_set_trace(void* buffer) { g_trace = static_cast<unsigned long lon
 #endif
 
 int32_t dsa_abi_version(void) { return 1; }
+
+int32_t dsa_set_tile_tokens(int32_t tile_tokens) {
+    if (tile_tokens != 0 && tile_tokens != 64 && tile_tokens != 128) return DSA_ERR_INVALID_ARGUMENT;
+    g_tile_tokens = tile_tokens;
+    return DSA_OK;
+}
 
 const char* dsa_status_string(int32_t status) {
     switch (status) {

@@ -12,13 +12,11 @@
 namespace dsa {
 
 constexpr int kLatent = 512;           // kv_lora_rank: the whole cache token (NoPE)
-constexpr int kTileTokens = 128;       // tokens per decode tile = MMA N of the score product
 constexpr int kCtaMinSlots = 128;      // default grid: at least this many slots per CTA
 constexpr int kHeadsPerCta = 64;       // query heads per work unit
 // Query operand image of one unit: 128 rows of 512 E4M3 codes, row 32*q + 2*k + t holding
 // term t (0 = hi, 1 = lo) of head 16*q + k, dims in natural order.
 constexpr int kQImageBytes = 2 * kHeadsPerCta * kLatent;  // 64 KB
-constexpr int kKvTileBytes = kTileTokens * kLatent;       // 64 KB of E4M3 per tile
 constexpr int kBitmapWords = 8192;     // resolve bitmap: seq_len up to 262144 tokens
 constexpr int kResolveThreads = 256;
 
@@ -165,9 +163,14 @@ struct CombineParams {
 // before them on the stream (they start their set-up early and wait on the grid
 // dependency before reading its results).
 cudaError_t launch_prologue(const PrologueParams& p, int blocks, cudaStream_t stream);
-cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
+// The decode kernel exists for tiles of 64 and of 128 tokens (decode.cu compiled twice);
+// 64-token tiles pipeline better when a CTA has little work, 128-token tiles use the
+// tensor core better when it has much.
+cudaError_t launch_decode_64(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_decode_128(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, int units, cudaStream_t stream);
-cudaError_t decode_kernel_setup();
+cudaError_t decode_kernel_setup_64();
+cudaError_t decode_kernel_setup_128();
 cudaError_t prologue_kernel_setup();
 cudaError_t combine_kernel_setup();
 

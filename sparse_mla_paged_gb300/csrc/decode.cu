@@ -39,8 +39,19 @@
 #include "common.cuh"
 #include "ptx.cuh"
 
+// This file is compiled once per tile size (DSA_TILE = 64 or 128); each build lives in its
+// own namespace and exports decode_kernel_setup_<tile> and launch_decode_<tile>.
+#ifndef DSA_TILE
+#define DSA_TILE 128
+#endif
+#define DSA_CAT2(a, b) a##b
+#define DSA_CAT(a, b) DSA_CAT2(a, b)
+
 namespace dsa {
-namespace {
+namespace DSA_CAT(tile, DSA_TILE) {
+
+constexpr int kTileTokens = DSA_TILE;                     // tokens per decode tile = MMA N of QK
+constexpr int kKvTileBytes = kTileTokens * kLatent;       // E4M3 bytes per tile
 
 constexpr int kProducerWarps = 3;
 constexpr int kMmaWarp = 3;
@@ -616,12 +627,14 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
         if (term == 0) l_s[half * kHeadsPerCta + hq] = lpair;
         named_bar_sync<kBarSoftmax, kSoftmaxThreads>();
         const bool whole = s.part < 0;
+        if (st == 0 && i == 0) DSA_TRACE_AT(p, 12);
         if (term == 0 && half == 0) {
             const float l = l_s[hq] + l_s[kHeadsPerCta + hq];
             f_s[hq] = (whole ? p.v_scale : 1.0f) / l;
             if (!whole) p.part_lse[s.part * kHeadsPerCta + hq] = m_ref + __log2f(l);
         }
         named_bar_sync<kBarSoftmax, kSoftmaxThreads>();
+        if (st == 0 && i == 0) DSA_TRACE_AT(p, 13);
 #pragma unroll 1
         for (int mc2 = 0; mc2 < 2; ++mc2) {
             const int mc = 2 * half + mc2;
@@ -630,6 +643,7 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
             for (int hh = 0; hh < 2; ++hh) {
                 uint32_t v[32];
                 tmem_ld_x32(tmem + lane_base + kTmemO + mc * 64 + hh * 32, v);
+                if (st == 0 && i == 0 && mc2 == 0 && hh == 0) DSA_TRACE_AT(p, 14);
                 float o[32], f[32];
 #pragma unroll
                 for (int k = 0; k < 32; ++k) {
@@ -647,6 +661,7 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
                 }
             }
         }
+        if (st == 0 && i == 0) DSA_TRACE_AT(p, 15);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(barp(BAR_OEMPTY));
@@ -738,9 +753,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     }
 }
 
-}  // namespace
+}  // namespace DSA_CAT(tile, DSA_TILE)
 
-cudaError_t decode_kernel_setup() {
+using namespace DSA_CAT(tile, DSA_TILE);
+
+cudaError_t DSA_CAT(decode_kernel_setup_, DSA_TILE)() {
     // The register cap above must leave room for all kThreads threads of the block.
     cudaFuncAttributes attr;
     cudaError_t e = cudaFuncGetAttributes(&attr, decode_kernel);
@@ -751,7 +768,7 @@ cudaError_t decode_kernel_setup() {
     return cudaFuncSetAttribute(decode_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
 }
 
-cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
+cudaError_t DSA_CAT(launch_decode_, DSA_TILE)(const DecodeParams& p, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.part.ctas);
     cfg.blockDim = dim3(kThreads);

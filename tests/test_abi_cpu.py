@@ -97,3 +97,10 @@ def test_workspace_size_grows_with_the_problem(lib):
     rows, width, ctas = 8, 2048, 152
     assert base >= rows * width * (4 + 8) + rows * 4 + rows * 65536 + 2 * ctas * 64 * 512 * 2
     assert f(0, 1, 64, 2048, 152) == 0
+
+
+def test_tile_tokens_knob_checks_its_argument(lib):
+    for bad in (-1, 1, 32, 96, 256):
+        assert lib.dsa_set_tile_tokens(bad) == 1
+    for good in (64, 128, 0):
+        assert lib.dsa_set_tile_tokens(good) == 0

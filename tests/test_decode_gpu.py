@@ -108,6 +108,18 @@ def test_decode_cases(api, name):
     _check(api, wl.random_case(seed=zlib.crc32(name.encode()) % 100000, **CASES[name]), name)
 
 
+@pytest.mark.parametrize("tile", [64, 128])
+@pytest.mark.parametrize("name", ["ragged 3 tiles", "many tiles", "130 heads", "block size 1", "split K/V many tiles",
+                                  "multi seq", "rows per seq", "heavy tails", "negative score scale"])
+def test_decode_cases_forced_tile(api, name, tile):
+    """Both builds of the decode kernel (64- and 128-token tiles) on the same inputs."""
+    api.set_tile_tokens(tile)
+    try:
+        _check(api, wl.random_case(seed=zlib.crc32(name.encode()) % 100000, **CASES[name]), f"{name} tile {tile}")
+    finally:
+        api.set_tile_tokens(0)
+
+
 @pytest.mark.parametrize("ctas", [1, 2, 3, 5, 17, 64, 152, 400])
 def test_decode_cta_counts(api, ctas):
     w = wl.random_case(num_seqs=4, heads=96, seq_lens=[2000, 100, 1500, 3000], sel_width=1000, seed=77)
