@@ -2,6 +2,7 @@
 // partition, workspace management and the launch sequence
 //   prologue (index resolution + query split) -> decode -> combine (when needed),
 // all enqueued on the caller's stream.
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -103,6 +104,7 @@ struct Plan {
     Partition part;
     bool any_split;
     bool small_tiles;  // 64-token tiles: at most two 128-slot tiles of work per CTA
+    int max_pieces;    // bound on the CTAs sharing one unit
     WsLayout ws;
 };
 
@@ -125,6 +127,20 @@ Plan make_plan(int64_t rows, int32_t heads, int32_t width, int32_t num_ctas, int
     pl.any_split = false;
     for (int64_t k = 1; k < c && !pl.any_split; ++k)
         if (cta_begin(pl.part, k) % width != 0) pl.any_split = true;
+    // CTAs sharing a unit: counted for up to 1024 units; otherwise bounded by the shortest
+    // CTA range, floor(T/C) slots, which a unit of W slots meets at most
+    // ceil((W - 1) / floor(T/C)) + 1 times (any number of times when ranges can be empty).
+    if (pl.units <= 1024) {
+        int64_t mp = 1;
+        for (int64_t u = 0; u < pl.units; ++u)
+            mp = std::max(mp, cta_of_slot(pl.part, (u + 1) * width - 1) - cta_of_slot(pl.part, u * width) + 1);
+        pl.max_pieces = static_cast<int>(std::min<int64_t>(mp, 1 << 20));
+    } else {
+        const int64_t min_range = pl.part.total_slots / c;
+        pl.max_pieces = min_range > 0 ? static_cast<int>(std::min<int64_t>(
+                                            (width - 1 + min_range - 1) / min_range + 1, 1 << 20))
+                                      : (1 << 20);
+    }
     pl.ws = ws_layout(rows, pl.groups, width, c);
     return pl;
 }
@@ -197,7 +213,7 @@ int32_t enqueue(const Args& a, const Plan& pl, uint8_t* ws, cudaEvent_t ev0, cud
         cp.part = pl.part;
         cp.heads = a.heads;
         cp.v_scale = a.v_scale;
-        st = from_cuda(launch_combine(cp, static_cast<int>(pl.units), stream));
+        st = from_cuda(launch_combine(cp, static_cast<int>(pl.units), pl.max_pieces, stream));
     }
     return st;
 }

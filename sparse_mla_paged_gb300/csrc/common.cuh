@@ -168,7 +168,8 @@ cudaError_t launch_prologue(const PrologueParams& p, int blocks, cudaStream_t st
 // tensor core better when it has much.
 cudaError_t launch_decode_64(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_decode_128(const DecodeParams& p, cudaStream_t stream);
-cudaError_t launch_combine(const CombineParams& p, int units, cudaStream_t stream);
+// max_pieces: an upper bound on the CTAs sharing one unit (selects the combine variant).
+cudaError_t launch_combine(const CombineParams& p, int units, int max_pieces, cudaStream_t stream);
 cudaError_t decode_kernel_setup_64();
 cudaError_t decode_kernel_setup_128();
 cudaError_t prologue_kernel_setup();

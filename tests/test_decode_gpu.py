@@ -128,6 +128,15 @@ def test_decode_cta_counts(api, ctas):
     assert api.read_device_status(ws) == 0
 
 
+@pytest.mark.parametrize("width,ctas", [(10, 15), (64, 100)])
+def test_more_ctas_than_slots(api, width, ctas):
+    """CTAs without slots leave no piece; the combine skips them."""
+    w = wl.random_case(heads=64, seq_len=300, sel_width=width, hole_frac=0.0, dup_frac=0.0, seed=width)
+    ws = api.alloc_workspace(1, 1, 64, width, num_ctas=ctas)
+    _check(api, w, f"{ctas} CTAs over {width} slots", workspace=ws, num_ctas=ctas, status_ok=False)
+    assert api.read_device_status(ws) == 0
+
+
 def test_empty_and_single_token_rows(api):
     w = wl.random_case(num_seqs=4, heads=64, seq_len=700, sel_width=300, hole_frac=0.0, dup_frac=0.0, seed=5)
     sel = w.sel_indices.clone()
