@@ -171,7 +171,8 @@ int32_t enqueue(const Args& a, const Plan& pl, uint8_t* ws, cudaEvent_t ev0, cud
     pp.rows_per_seq = a.rows_per_seq;
     pp.verify_rows = a.verify_rows;
     pp.score_scale = a.sm_scale * a.k_scale * 1.4426950408889634f;
-    int32_t st = from_cuda(launch_prologue(pp, static_cast<int>(pl.rows + pl.units), stream));
+    const bool early = pl.part.total_slots >= kEarlyDependentSlots * pl.part.ctas;
+    int32_t st = from_cuda(launch_prologue(pp, static_cast<int>(pl.rows + pl.units), early, stream));
     if (st != DSA_OK) return st;
 
     DecodeParams dp{};
@@ -189,6 +190,7 @@ int32_t enqueue(const Args& a, const Plan& pl, uint8_t* ws, cudaEvent_t ev0, cud
     dp.heads = a.heads;
     dp.kv_same = a.k_cache == a.v_cache ? 1 : 0;
     dp.v_scale = a.v_scale;
+    dp.early_dependents = early ? 1 : 0;
 #ifdef DSA_TRACE
     dp.trace = g_trace;
 #endif
@@ -213,6 +215,7 @@ int32_t enqueue(const Args& a, const Plan& pl, uint8_t* ws, cudaEvent_t ev0, cud
         cp.part = pl.part;
         cp.heads = a.heads;
         cp.v_scale = a.v_scale;
+        cp.early_dependents = dp.early_dependents;
         st = from_cuda(launch_combine(cp, static_cast<int>(pl.units), pl.max_pieces, stream));
     }
     return st;
@@ -460,7 +463,7 @@ int32_t dsa_resolve_indices(const int32_t* sel_indices, const int32_t* seq_lens,
     pp.heads = 1;
     pp.groups = 1;
     pp.rows_per_seq = 1;
-    return from_cuda(launch_prologue(pp, rows, static_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_prologue(pp, rows, false, static_cast<cudaStream_t>(stream)));
 }
 
 int32_t dsa_read_device_status(const void* workspace, int32_t* status_out, void* stream) {

@@ -50,6 +50,9 @@ __device__ __forceinline__ void store_head(const CombineParams& p, int32_t r, in
 // loads at a time. The variants differ in registers, hence in blocks per SM.
 template <int kFastPieces>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams p) {
+    // After a long decode the next call's first kernel may launch now (it waits for this
+    // grid to complete); otherwise it launches when this grid exits.
+    if (p.early_dependents) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __shared__ int32_t slot_s[kCombineThreads];
     __shared__ float lse_s[kCombineHeads][kCombineThreads];
     const int64_t u = blockIdx.x;

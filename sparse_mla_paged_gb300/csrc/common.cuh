@@ -13,6 +13,9 @@ namespace dsa {
 
 constexpr int kLatent = 512;           // kv_lora_rank: the whole cache token (NoPE)
 constexpr int kCtaMinSlots = 128;      // default grid: at least this many slots per CTA
+// From this many slots per decode CTA on, the decode and combine kernels let the next
+// kernel on the stream launch early (measured: a gain on long decodes, a loss on short).
+constexpr int64_t kEarlyDependentSlots = 2048;
 constexpr int kHeadsPerCta = 64;       // query heads per work unit
 // Query operand image of one unit: 128 rows of 512 E4M3 codes, row 32*q + 2*k + t holding
 // term t (0 = hi, 1 = lo) of head 16*q + k, dims in natural order.
@@ -146,6 +149,7 @@ struct DecodeParams {
     int32_t heads;
     int32_t kv_same;
     float v_scale;
+    int32_t early_dependents;  // let the next kernel launch once every CTA has started
     unsigned long long* trace;  // per-CTA timeline, used only by -DDSA_TRACE builds
 };
 
@@ -156,13 +160,16 @@ struct CombineParams {
     Partition part;
     int32_t heads;
     float v_scale;
+    int32_t early_dependents;  // let the next kernel launch as soon as every block has started
 };
 
 // Launchers (each defined next to its kernel).
 // The decode and combine kernels are launched as programmatic dependents of the kernel
 // before them on the stream (they start their set-up early and wait on the grid
 // dependency before reading its results).
-cudaError_t launch_prologue(const PrologueParams& p, int blocks, cudaStream_t stream);
+// programmatic: launch as a programmatic dependent of the kernel before it (done after long
+// decodes, whose decode and combine kernels let their dependents launch early).
+cudaError_t launch_prologue(const PrologueParams& p, int blocks, bool programmatic, cudaStream_t stream);
 // The decode kernel exists for tiles of 64 and of 128 tokens (decode.cu compiled twice);
 // 64-token tiles pipeline better when a CTA has little work, 128-token tiles use the
 // tensor core better when it has much.

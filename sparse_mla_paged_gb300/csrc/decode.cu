@@ -716,6 +716,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     // Everything above overlaps the prologue; its results are read only after this.
     griddep_wait();
     if (tid == 0) DSA_TRACE_AT(p, 1);
+    // Long decodes let the next kernel on the stream launch once every CTA has passed here
+    // (it waits for this grid's completion before reading its results); short ones at the end.
+    if (p.early_dependents) griddep_launch_dependents();
 
     int64_t first_unit;
     const int nseg = cta_segments(p.part, blockIdx.x, &first_unit);
@@ -746,7 +749,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     tc_fence_before();
     __syncthreads();
     if (tid == 0) DSA_TRACE_AT(p, 20);
-    griddep_launch_dependents();
+    if (!p.early_dependents) griddep_launch_dependents();
     if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);

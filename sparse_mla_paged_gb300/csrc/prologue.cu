@@ -250,6 +250,9 @@ __device__ void prepare_queries(const PrologueParams& p, int32_t unit) {
 __global__ void __launch_bounds__(kResolveThreads) prologue_kernel(const PrologueParams p) {
     extern __shared__ __align__(16) uint32_t bitmap[];  // kBitmapWords words, then kMaxSel ids
     __shared__ int32_t scratch[kResolveThreads / 32];
+    // When launched as a programmatic dependent of the kernel before it on the stream,
+    // nothing is read or written before that kernel has completed.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // Let the decode kernel launch and run its set-up while this grid finishes; it waits
     // for this grid's completion before reading anything written here.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -273,10 +276,23 @@ cudaError_t prologue_kernel_setup() {
     return cudaFuncSetAttribute(prologue_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
 }
 
-cudaError_t launch_prologue(const PrologueParams& p, int blocks, cudaStream_t stream) {
+cudaError_t launch_prologue(const PrologueParams& p, int blocks, bool programmatic, cudaStream_t stream) {
     if (blocks <= 0) return cudaSuccess;
-    prologue_kernel<<<blocks, kResolveThreads, kPrologueSmem, stream>>>(p);
-    return cudaGetLastError();
+    if (!programmatic) {
+        prologue_kernel<<<blocks, kResolveThreads, kPrologueSmem, stream>>>(p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(kResolveThreads);
+    cfg.dynamicSmemBytes = kPrologueSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prologue_kernel, p);
 }
 
 }  // namespace dsa
