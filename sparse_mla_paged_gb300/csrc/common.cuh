@@ -65,8 +65,9 @@ __host__ __device__ inline WsLayout ws_layout(int64_t rows, int64_t groups, int6
 // A work unit is (row r, head group g) with sel_width "slots"; units are ordered
 // u = r*groups + g. The concatenated slot space [0, T), T = units*sel_width, is cut into
 // num_ctas contiguous ranges [c*T/C, (c+1)*T/C). A unit's slot range [s0, s1) maps to
-// resolved-token range [s0*U/W, s1*U/W) of that row (U = resolved count), so ranges of
-// neighbouring CTAs abut exactly whatever U is. A unit covered by one CTA is written
+// positions [min(s0, U), min(s1, U)) of that row's resolved list (U = resolved count), so
+// ranges of neighbouring CTAs abut exactly whatever U is, and a CTA can request its
+// first tokens before it knows U. A unit covered by one CTA is written
 // straight to the output; a unit shared by several CTAs leaves per-CTA partials (slot
 // 2c for the CTA's first unit, 2c+1 for its last) that the combine kernel merges.
 // ------------------------------------------------------------------------------------

@@ -126,12 +126,13 @@ struct Tiles {
     int32_t ntiles;
 };
 
+// Resolved tokens of a segment: positions [s0, s1) of the row's resolved list, clipped to
+// its count U (the list holds the U distinct ids first).
 __device__ __forceinline__ Tiles segment_tokens(const DecodeParams& p, const Segment& s) {
     const int64_t U = p.cnt[s.row];
-    const int64_t W = p.part.width;
     Tiles t;
-    t.t0 = s.s0 * U / W;
-    const int64_t t1 = s.s1 * U / W;
+    t.t0 = s.s0 < U ? s.s0 : U;
+    const int64_t t1 = s.s1 < U ? s.s1 : U;
     t.n = static_cast<int32_t>(t1 - t.t0);
     t.ntiles = (t.n + kTileTokens - 1) / kTileTokens;
     return t;
@@ -193,18 +194,24 @@ __device__ void run_producer(const DecodeParams& p, uint32_t sbase, volatile int
     for (int i = 0; i < nseg; ++i) {
         const Segment s = cta_segment(p.part, blockIdx.x, i);
         if (tid == 0 && i == 0) DSA_TRACE_AT(p, 3);
+        // The segment's tokens start at position s0 of the row's resolved list, so the first
+        // tile's offsets are requested together with the row's count (positions past the
+        // count hold stale values and are masked once it arrives).
+        const long long* offs = p.offs + static_cast<int64_t>(s.row) * W + s.s0;
+        const int32_t span = static_cast<int32_t>(s.s1 - s.s0);
+        const long long pa = (r0 + lane < span) ? offs[r0 + lane] : -1;
+        const long long pb = (lane + 32 < nr && r0 + 32 + lane < span) ? offs[r0 + 32 + lane] : -1;
         const Tiles tl = segment_tokens(p, s);
         if (tid == 0 && i == 0 && tl.n >= 0) DSA_TRACE_AT(p, 4);
         if (tl.n <= 0) continue;
-        const long long* offs = p.offs + static_cast<int64_t>(s.row) * W + tl.t0;
         // This lane's rows of tile t: r0 + lane and r0 + 32 + lane (the latter for lane < nr - 32).
         auto load = [&](int t, long long& a, long long& b) {
             const int ta = t * kTileTokens + r0 + lane, tb = ta + 32;
             a = (t < tl.ntiles && ta < tl.n) ? offs[ta] : -1;
             b = (t < tl.ntiles && lane + 32 < nr && tb < tl.n) ? offs[tb] : -1;
         };
-        long long oa, ob;
-        load(0, oa, ob);
+        long long oa = (r0 + lane < tl.n) ? pa : -1;
+        long long ob = (lane + 32 < nr && r0 + 32 + lane < tl.n) ? pb : -1;
         for (int t = 0; t < tl.ntiles; ++t, ++tau) {
             const long long ca = oa, cb = ob;
             if (tid == 0 && t == 0 && i == 0 && ca != 12345) DSA_TRACE_AT(p, 5);
@@ -639,17 +646,23 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
         for (int mc2 = 0; mc2 < 2; ++mc2) {
             const int mc = 2 * half + mc2;
             const int dim0 = mc * 128 + q4 * 32;
-#pragma unroll 1
+            // All 64 head columns of this lane's dim in one load and one wait.
+            uint32_t v64[64];
+            tmem_ld_x64(tmem + lane_base + kTmemO + mc * 64, v64);
+            if (st == 0 && i == 0 && mc2 == 0) DSA_TRACE_AT(p, 14);
+#pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-                uint32_t v[32];
-                tmem_ld_x32(tmem + lane_base + kTmemO + mc * 64 + hh * 32, v);
-                if (st == 0 && i == 0 && mc2 == 0 && hh == 0) DSA_TRACE_AT(p, 14);
                 float o[32], f[32];
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    o[k] = __uint_as_float(v[k]);
-                    f[k] = f_s[hh * 32 + k];
+                for (int k = 0; k < 32; k += 4) {
+                    const float4 f4 = *reinterpret_cast<const float4*>(f_s + hh * 32 + k);
+                    f[k] = f4.x;
+                    f[k + 1] = f4.y;
+                    f[k + 2] = f4.z;
+                    f[k + 3] = f4.w;
                 }
+#pragma unroll
+                for (int k = 0; k < 32; ++k) o[k] = __uint_as_float(v64[hh * 32 + k]);
                 if (whole) {
                     __nv_bfloat16* rows = reinterpret_cast<__nv_bfloat16*>(p.out) + head0 * kLatent;
                     store_block(rows, hh * 32, hvalid, dim0, o, f, stage, lane);
