@@ -159,7 +159,7 @@ int32_t enqueue(const Args& a, const Plan& pl, uint8_t* ws, cudaEvent_t ev0, cud
     for (int s = 0; s < 31; ++s)
         if ((1 << s) == a.block_size) pp.block_shift = s;
     pp.max_blocks_per_seq = a.max_blocks_per_seq;
-    pp.ids = reinterpret_cast<int32_t*>(ws + pl.ws.ids);
+    pp.ids = nullptr;
     pp.cnt = reinterpret_cast<int32_t*>(ws + pl.ws.cnt);
     pp.qimg = ws + pl.ws.qimg;
     pp.qscale = reinterpret_cast<float*>(ws + pl.ws.qscale);

@@ -39,7 +39,7 @@ constexpr int kStatusTimeout = DSA_ERR_TIMEOUT;
 // Workspace layout (all offsets 256-byte aligned).
 // ------------------------------------------------------------------------------------
 struct WsLayout {
-    size_t status, ids, offs, cnt, qimg, qscale, part_o, part_lse, total;
+    size_t status, offs, cnt, qimg, qscale, part_o, part_lse, total;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -48,7 +48,6 @@ __host__ __device__ inline WsLayout ws_layout(int64_t rows, int64_t groups, int6
     WsLayout L;
     size_t o = 0;
     L.status = o; o += 256;
-    L.ids = o; o = align256(o + static_cast<size_t>(rows * width) * 4);
     L.offs = o; o = align256(o + static_cast<size_t>(rows * width) * 8);
     L.cnt = o; o = align256(o + static_cast<size_t>(rows) * 4);
     L.qimg = o; o = align256(o + static_cast<size_t>(rows * groups) * kQImageBytes);
@@ -123,7 +122,7 @@ struct PrologueParams {
     const int32_t* seq_lens;   // [R] or [num_seqs] (verify rows)
     const uint16_t* q;         // bf16 bits [R, H, 512]; null: resolve only
     const int32_t* block_tables;  // null: ids only, no byte offsets
-    int32_t* ids;              // [R, W]
+    int32_t* ids;              // [R, W], or null: the decode needs only offs and cnt
     long long* offs;           // [R, W] cache byte offset of each resolved token (-1: bad page)
     int32_t* cnt;              // [R]
     uint8_t* qimg;             // [R*G, 64 KB]

@@ -25,6 +25,7 @@ namespace {
 
 constexpr int kMaxSel = DSA_MAX_SEL_WIDTH;                        // resolved ids per row, at most
 constexpr int kPrologueSmem = kBitmapWords * 4 + kMaxSel * 4;     // bitmap or keys, then the ids
+static_assert(kQImageBytes <= kPrologueSmem, "a query block stages its image in the same shared memory");
 constexpr int kBatch = 8;                                         // loads in flight per thread
 
 __device__ __forceinline__ int32_t row_seq_len(const PrologueParams& p, int32_t r) {
@@ -78,7 +79,7 @@ __device__ void resolve_row(const PrologueParams& p, int32_t r, uint32_t* sm, in
     const int32_t L = row_seq_len(p, r);
     const int32_t seq = r / p.rows_per_seq;
     const int32_t* sel = p.sel + static_cast<int64_t>(r) * W;
-    int32_t* ids = p.ids + static_cast<int64_t>(r) * W;
+    int32_t* ids = p.ids ? p.ids + static_cast<int64_t>(r) * W : nullptr;
     long long* offs = p.block_tables ? p.offs + static_cast<int64_t>(r) * W : nullptr;
     int32_t total = 0;
     if (L <= kBitmapWords * 32) {
@@ -159,7 +160,8 @@ __device__ void resolve_row(const PrologueParams& p, int32_t r, uint32_t* sm, in
     __syncthreads();
     // Coalesced write-out of the ids (-1 padded), then each id's byte offset with all of a
     // thread's block-table loads in flight at once.
-    for (int32_t j = tid; j < W; j += kResolveThreads) ids[j] = j < total ? ids_s[j] : -1;
+    if (ids)
+        for (int32_t j = tid; j < W; j += kResolveThreads) ids[j] = j < total ? ids_s[j] : -1;
     if (tid == 0) p.cnt[r] = total;
     if (!offs) return;
     for (int32_t j0 = tid; j0 < total; j0 += kBatch * kResolveThreads) {
@@ -177,8 +179,11 @@ __device__ void resolve_row(const PrologueParams& p, int32_t r, uint32_t* sm, in
     }
 }
 
-// One (row, group): 8 warps x 8 heads; lane l handles latent dims [16l, 16l+16).
-__device__ void prepare_queries(const PrologueParams& p, int32_t unit) {
+// One (row, group): 8 warps x 8 heads; lane l handles latent dims [16l, 16l+16). The
+// image is assembled in shared memory (row r's chunk c at r*512 + (c ^ (r % 32))*16, so
+// that both the row writes and the chunk reads below are free of bank conflicts) and then
+// written out chunk-major with each warp storing 512 contiguous bytes.
+__device__ void prepare_queries(const PrologueParams& p, int32_t unit, uint8_t* stage) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int32_t r = unit / p.groups, g = unit % p.groups;
     uint8_t* img = p.qimg + static_cast<int64_t>(unit) * kQImageBytes;
@@ -239,11 +244,19 @@ __device__ void prepare_queries(const PrologueParams& p, int32_t unit) {
         // chunk-major ([32 chunks of 16 bytes][128 rows][16 bytes]): 32 consecutive rows of
         // one chunk are 512 contiguous bytes, which the decode reads one row per lane.
         const int rh = 32 * (hl >> 4) + 2 * (hl & 15);
-        *reinterpret_cast<uint4*>(img + lane * 2048 + rh * 16) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(img + lane * 2048 + (rh + 1) * 16) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        *reinterpret_cast<uint4*>(stage + rh * 512 + ((lane ^ (rh & 31)) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(stage + (rh + 1) * 512 + ((lane ^ ((rh + 1) & 31)) << 4)) =
+            make_uint4(lo[0], lo[1], lo[2], lo[3]);
         if (lane == 0)
             p.qscale[static_cast<int64_t>(unit) * kHeadsPerCta + hl] =
                 p.score_scale * __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+    }
+    __syncthreads();
+    // 4096 16-byte pieces; piece k is chunk k / 128 of row k % 128.
+    for (int k = threadIdx.x; k < kQImageBytes / 16; k += kResolveThreads) {
+        const int c = k >> 7, r = k & 127;
+        *reinterpret_cast<uint4*>(img + c * 2048 + r * 16) =
+            *reinterpret_cast<const uint4*>(stage + r * 512 + ((c ^ (r & 31)) << 4));
     }
 }
 
@@ -260,7 +273,7 @@ __global__ void __launch_bounds__(kResolveThreads) prologue_kernel(const Prologu
     if (static_cast<int32_t>(blockIdx.x) < p.rows)
         resolve_row(p, blockIdx.x, bitmap, reinterpret_cast<int32_t*>(bitmap + kBitmapWords), scratch);
     else
-        prepare_queries(p, blockIdx.x - p.rows);
+        prepare_queries(p, blockIdx.x - p.rows, reinterpret_cast<uint8_t*>(bitmap));
 }
 
 }  // namespace
