@@ -60,18 +60,6 @@ __device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t* scra
     return before;
 }
 
-// Byte offset of token `id` of sequence `seq` in the cache, or -1 when the block table
-// has no valid page for it (the decode kernel reports that as a device status).
-__device__ __forceinline__ long long token_offset(const PrologueParams& p, int32_t seq, int32_t id) {
-    const int32_t blk = p.block_shift >= 0 ? (id >> p.block_shift) : id / p.block_size;
-    const int32_t inblk = id - blk * p.block_size;
-    if (p.max_blocks_per_seq > 0 && blk >= p.max_blocks_per_seq) return -1;
-    const int32_t page = p.block_tables[static_cast<int64_t>(seq) * p.max_blocks_per_seq + blk];
-    if (page < 0) return -1;
-    return static_cast<long long>(page) * p.cache_stride + static_cast<long long>(inblk) * kLatent;
-}
-
-
 // sm: kBitmapWords words of scratch (bitmap or sort keys); ids_s: kMaxSel resolved ids.
 __device__ void resolve_row(const PrologueParams& p, int32_t r, uint32_t* sm, int32_t* ids_s, int32_t* scratch) {
     const int tid = threadIdx.x;
@@ -165,16 +153,29 @@ __device__ void resolve_row(const PrologueParams& p, int32_t r, uint32_t* sm, in
     if (tid == 0) p.cnt[r] = total;
     if (!offs) return;
     for (int32_t j0 = tid; j0 < total; j0 += kBatch * kResolveThreads) {
-        long long o[kBatch];
+        // Cache byte offset of each id through the block table (decode_k.rs: physical =
+        // block_table[pos / block_size], slot = physical*block_size + pos % block_size),
+        // -1 when the table has no valid page for it (the decode kernel reports that as a
+        // device status). All of the batch's table loads are issued (predicated, with no
+        // branch between them) before any of their results is used.
+        int32_t id[kBatch], page[kBatch];
 #pragma unroll
         for (int e = 0; e < kBatch; ++e) {
             const int32_t j = j0 + e * kResolveThreads;
-            o[e] = j < total ? token_offset(p, seq, ids_s[j]) : 0;
+            id[e] = j < total ? ids_s[j] : 0;
+            const int32_t blk = p.block_shift >= 0 ? (id[e] >> p.block_shift) : id[e] / p.block_size;
+            const bool ok = j < total && (p.max_blocks_per_seq <= 0 || blk < p.max_blocks_per_seq);
+            page[e] = ok ? p.block_tables[static_cast<int64_t>(seq) * p.max_blocks_per_seq + blk] : -1;
         }
 #pragma unroll
         for (int e = 0; e < kBatch; ++e) {
             const int32_t j = j0 + e * kResolveThreads;
-            if (j < total) offs[j] = o[e];
+            if (j < total) {
+                const int32_t inblk = p.block_shift >= 0 ? (id[e] & (p.block_size - 1)) : id[e] % p.block_size;
+                offs[j] = page[e] >= 0 ? static_cast<long long>(page[e]) * p.cache_stride +
+                                             static_cast<long long>(inblk) * kLatent
+                                       : -1ll;
+            }
         }
     }
 }
