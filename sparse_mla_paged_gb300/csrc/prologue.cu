@@ -70,15 +70,16 @@ __device__ void resolve_row(const PrologueParams& p, int32_t r, uint32_t* sm, in
     int32_t* ids = p.ids ? p.ids + static_cast<int64_t>(r) * W : nullptr;
     long long* offs = p.block_tables ? p.offs + static_cast<int64_t>(r) * W : nullptr;
     int32_t total = 0;
+    // The first batch of the selection row is requested together with the row's length
+    // (before the branch on it), and arrives while the bitmap is cleared.
+    int32_t idv[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+        const int32_t j = tid + k * kResolveThreads;
+        idv[k] = j < W ? sel[j] : -1;
+    }
     if (L <= kBitmapWords * 32) {
         const int32_t nwords = (L + 31) >> 5;
-        // The first batch of the selection row is loaded while the bitmap is cleared.
-        int32_t idv[kBatch];
-#pragma unroll
-        for (int k = 0; k < kBatch; ++k) {
-            const int32_t j = tid + k * kResolveThreads;
-            idv[k] = j < W ? sel[j] : -1;
-        }
         for (int32_t w = tid; w < nwords; w += kResolveThreads) sm[w] = 0u;
         __syncthreads();
         for (int32_t j0 = tid;; j0 += kBatch * kResolveThreads) {
