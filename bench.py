@@ -39,7 +39,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one decode-kernel launch, from the ncu capture of the
 # current kernel summarised under profiles/ (decode_kernel_<workload>.md). A workload
 # absent here reports traffic null; an entry is removed whenever the kernel changes.
-MEASURED_TRAFFIC = {"decode_batch": 8944128, "ragged": 72939264 + 2277120}
+MEASURED_TRAFFIC = {}
 
 
 # ----------------------------------------------------------------------------------------

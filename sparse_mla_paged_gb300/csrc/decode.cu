@@ -183,7 +183,8 @@ struct Ring {
 // Rows of a tile taken by gather warp w: [w*43, min(w*43 + 43, 128)).
 constexpr int kWarpRows = (kTileTokens + kProducerWarps - 1) / kProducerWarps;
 
-__device__ void run_producer(const DecodeParams& p, uint32_t sbase, volatile int* abort_flag, int nseg) {
+__device__ void run_producer(const DecodeParams& p, uint32_t sbase, volatile int* abort_flag, int nseg,
+                             const Segment& seg0) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const Ring ring(p.kv_same);
     const int64_t W = p.part.width;
@@ -192,7 +193,7 @@ __device__ void run_producer(const DecodeParams& p, uint32_t sbase, volatile int
     uint32_t tau = 0;
     if (tid == 0) DSA_TRACE_AT(p, 2);
     for (int i = 0; i < nseg; ++i) {
-        const Segment s = cta_segment(p.part, blockIdx.x, i);
+        const Segment s = i == 0 ? seg0 : cta_segment(p.part, blockIdx.x, i);
         if (tid == 0 && i == 0) DSA_TRACE_AT(p, 3);
         // The segment's tokens start at position s0 of the row's resolved list, so the first
         // tile's offsets are requested together with the row's count (positions past the
@@ -290,7 +291,8 @@ __device__ __forceinline__ void mma_wait(const DecodeParams& p, uint32_t bar, ui
 }
 
 // The whole MMA warp runs this loop converged; the elected lane issues.
-__device__ void run_mma(const DecodeParams& p, uint32_t sbase, uint32_t tmem, volatile int* abort_flag, int nseg) {
+__device__ void run_mma(const DecodeParams& p, uint32_t sbase, uint32_t tmem, volatile int* abort_flag, int nseg,
+                        const Segment& seg0) {
     const Ring ring(p.kv_same);
     const uint32_t idq = idesc_e4m3(128, kTileTokens, false, false);
     const uint32_t idp = idesc_e4m3(128, kHeadsPerCta, true, false);
@@ -355,7 +357,7 @@ __device__ void run_mma(const DecodeParams& p, uint32_t sbase, uint32_t tmem, vo
 
     uint32_t tau = 0;
     for (int i = 0; i < nseg; ++i) {
-        const Segment s = cta_segment(p.part, blockIdx.x, i);
+        const Segment s = i == 0 ? seg0 : cta_segment(p.part, blockIdx.x, i);
         const Tiles tl = segment_tokens(p, s);
         if (tl.n <= 0) continue;
         mma_wait(p, barp(BAR_QFULL), qseg & 1, abort_flag);
@@ -436,7 +438,7 @@ __device__ __forceinline__ void store_block(T* rows, int h0, int hvalid, int dim
 }
 
 __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase, uint32_t tmem,
-                            volatile int* abort_flag, int nseg) {
+                            volatile int* abort_flag, int nseg, const Segment& seg0) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int sw = warp - kSoftmaxWarp0;      // 0..7
     const int q4 = warp & 3;                  // TMEM lane quarter of this warp
@@ -483,7 +485,7 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
         if (lane == 0) mbar_arrive(barp(BAR_QFULL));
     };
     for (int i = 0; i < nseg; ++i) {
-        const Segment s = cta_segment(p.part, blockIdx.x, i);
+        const Segment s = i == 0 ? seg0 : cta_segment(p.part, blockIdx.x, i);
         const Tiles tl = segment_tokens(p, s);
         const int hvalid = min(kHeadsPerCta, p.heads - s.group * kHeadsPerCta);
         const int64_t head0 = static_cast<int64_t>(s.row) * p.heads + s.group * kHeadsPerCta;
@@ -726,6 +728,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmemSlot);
+    // The partition is arithmetic on the launch parameters (64-bit divisions): the first
+    // segment is worked out here, overlapping the prologue, and pinned before the wait.
+    int64_t first_unit;
+    const int nseg = cta_segments(p.part, blockIdx.x, &first_unit);
+    const Segment seg0 = cta_segment(p.part, blockIdx.x, 0);
+    asm volatile("" ::"r"(nseg), "r"(seg0.unit), "r"(seg0.row), "r"(seg0.group), "l"(seg0.s0), "l"(seg0.s1),
+                 "r"(seg0.part));
     // Everything above overlaps the prologue; its results are read only after this.
     griddep_wait();
     if (tid == 0) DSA_TRACE_AT(p, 1);
@@ -733,13 +742,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     // (it waits for this grid's completion before reading its results); short ones at the end.
     if (p.early_dependents) griddep_launch_dependents();
 
-    int64_t first_unit;
-    const int nseg = cta_segments(p.part, blockIdx.x, &first_unit);
-
     if (warp < kProducerWarps) {
-        run_producer(p, sbase, abort_flag, nseg);
+        run_producer(p, sbase, abort_flag, nseg, seg0);
     } else if (warp == kMmaWarp) {
-        run_mma(p, sbase, tmem, abort_flag, nseg);
+        run_mma(p, sbase, tmem, abort_flag, nseg, seg0);
         // Wait (bounded, regardless of abort) until every issued MMA has completed and the
         // softmax warps have finished reading TMEM.
         const uint32_t db = sbase + kOffBars + 8 * BAR_DRAIN;
@@ -754,7 +760,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
         }
         __syncwarp();
     } else {
-        run_softmax(p, smem, sbase, tmem, abort_flag, nseg);
+        run_softmax(p, smem, sbase, tmem, abort_flag, nseg, seg0);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(sbase + kOffBars + 8 * BAR_DONE);
