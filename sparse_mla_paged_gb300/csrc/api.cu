@@ -127,20 +127,7 @@ Plan make_plan(int64_t rows, int32_t heads, int32_t width, int32_t num_ctas, int
     pl.any_split = false;
     for (int64_t k = 1; k < c && !pl.any_split; ++k)
         if (cta_begin(pl.part, k) % width != 0) pl.any_split = true;
-    // CTAs sharing a unit: counted for up to 1024 units; otherwise bounded by the shortest
-    // CTA range, floor(T/C) slots, which a unit of W slots meets at most
-    // ceil((W - 1) / floor(T/C)) + 1 times (any number of times when ranges can be empty).
-    if (pl.units <= 1024) {
-        int64_t mp = 1;
-        for (int64_t u = 0; u < pl.units; ++u)
-            mp = std::max(mp, cta_of_slot(pl.part, (u + 1) * width - 1) - cta_of_slot(pl.part, u * width) + 1);
-        pl.max_pieces = static_cast<int>(std::min<int64_t>(mp, 1 << 20));
-    } else {
-        const int64_t min_range = pl.part.total_slots / c;
-        pl.max_pieces = min_range > 0 ? static_cast<int>(std::min<int64_t>(
-                                            (width - 1 + min_range - 1) / min_range + 1, 1 << 20))
-                                      : (1 << 20);
-    }
+    pl.max_pieces = static_cast<int>(std::min<int64_t>(max_pieces_bound(pl.part), 1 << 20));
     pl.ws = ws_layout(rows, pl.groups, width, c);
     return pl;
 }

@@ -114,6 +114,24 @@ __host__ __device__ inline Segment cta_segment(const Partition& p, int64_t c, in
     return s;
 }
 
+// Bound on the CTAs sharing one unit: counted for up to 1024 units (CTAs with an empty
+// range inside a unit included); otherwise from the shortest CTA range, floor(T/C) slots,
+// which a unit of W slots meets at most ceil((W - 1) / floor(T/C)) + 1 times (up to C
+// times when ranges can be empty).
+inline int64_t max_pieces_bound(const Partition& p) {
+    const int64_t units = p.total_slots / p.width;
+    if (units <= 1024) {
+        int64_t mp = 1;
+        for (int64_t u = 0; u < units; ++u) {
+            const int64_t k = cta_of_slot(p, (u + 1) * p.width - 1) - cta_of_slot(p, u * p.width) + 1;
+            mp = k > mp ? k : mp;
+        }
+        return mp;
+    }
+    const int64_t min_range = p.total_slots / p.ctas;
+    return min_range > 0 ? (p.width - 1 + min_range - 1) / min_range + 1 : p.ctas;
+}
+
 // ------------------------------------------------------------------------------------
 // Kernel parameter blocks.
 // ------------------------------------------------------------------------------------
