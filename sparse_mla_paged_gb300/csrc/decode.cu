@@ -405,19 +405,20 @@ __device__ void run_mma(const DecodeParams& p, uint32_t sbase, uint32_t tmem, vo
 // softmax / epilogue warps
 // ------------------------------------------------------------------------------------
 
-// Writes a warp's 32 dims x 16 heads block (dims on lanes, v[k] = head h0+k, scaled by
-// f[k]) to row-major global rows (row stride kLatent elements) through a 2 KB per-warp
-// staging area, with 16-byte stores. T is bf16 (output) or f16 (partials). Heads at or
-// beyond hvalid are not written.
+// Writes a warp's 32 dims x 32 heads block (dims on lanes, v[k] = head h0+k, scaled by
+// f[k]) to row-major global rows (row stride kLatent elements) through the warp's 2 KB
+// staging area (one staging round for all 32 heads), with 16-byte stores. T is bf16
+// (output) or f16 (partials). Heads at or beyond hvalid are not written.
 template <typename T>
 __device__ __forceinline__ void store_block(T* rows, int h0, int hvalid, int dim0, const float* v, const float* f,
                                             uint8_t* stage, int lane) {
     constexpr int kPer16 = 16 / static_cast<int>(sizeof(T));  // elements per 16-byte store
     constexpr int kLanesPerRow = 32 / kPer16;                 // lanes covering one head's 32 dims
     constexpr int kRowsPerPass = 32 / kLanesPerRow;           // heads per warp-wide store
-    T* stg = reinterpret_cast<T*>(stage);                     // [16 heads][32 dims]
+    static_assert(32 * 32 * sizeof(T) <= 2048, "staging area");
+    T* stg = reinterpret_cast<T*>(stage);                     // [32 heads][32 dims]
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
+    for (int k = 0; k < 32; ++k) {
         const float x = v[k] * f[k];
         if constexpr (std::is_same<T, __half>::value) {
             stg[k * 32 + lane] = __float2half_rn(x);
@@ -427,7 +428,7 @@ __device__ __forceinline__ void store_block(T* rows, int h0, int hvalid, int dim
     }
     __syncwarp();
 #pragma unroll
-    for (int pass = 0; pass < 16 / kRowsPerPass; ++pass) {
+    for (int pass = 0; pass < 32 / kRowsPerPass; ++pass) {
         const int hk = pass * kRowsPerPass + lane / kLanesPerRow;
         const int c = (lane % kLanesPerRow) * kPer16;
         const uint4 val = *reinterpret_cast<const uint4*>(stg + hk * 32 + c);
@@ -450,6 +451,7 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
     float* alpha_s = reinterpret_cast<float*>(smem + kOffAlpha);
     float* l_s = reinterpret_cast<float*>(smem + kOffL);
     float* f_s = reinterpret_cast<float*>(smem + kOffF);
+    static_assert(kSoftmaxWarps * 2048 <= 4 * kPTermBytes, "epilogue staging fits the P buffers");
     uint8_t* stage = smem + kOffP + sw * 2048;  // epilogue staging (2 KB per warp)
     auto barp = [&](int b) { return sbase + kOffBars + 8 * b; };
     const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
@@ -668,11 +670,9 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
                 if (whole) {
                     __nv_bfloat16* rows = reinterpret_cast<__nv_bfloat16*>(p.out) + head0 * kLatent;
                     store_block(rows, hh * 32, hvalid, dim0, o, f, stage, lane);
-                    store_block(rows, hh * 32 + 16, hvalid, dim0, o + 16, f + 16, stage, lane);
                 } else {
                     __half* rows = reinterpret_cast<__half*>(p.part_o) + static_cast<int64_t>(s.part) * kHeadsPerCta * kLatent;
                     store_block(rows, hh * 32, kHeadsPerCta, dim0, o, f, stage, lane);
-                    store_block(rows, hh * 32 + 16, kHeadsPerCta, dim0, o + 16, f + 16, stage, lane);
                 }
             }
         }
