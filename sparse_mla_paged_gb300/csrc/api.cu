@@ -104,7 +104,7 @@ struct Plan {
     Partition part;
     bool any_split;
     bool small_tiles;  // 64-token tiles: at most two 128-slot tiles of work per CTA
-    int max_pieces;    // bound on the CTAs sharing one unit
+    int max_pieces;    // most CTAs sharing one unit (selects the combine variant)
     WsLayout ws;
 };
 
@@ -127,7 +127,7 @@ Plan make_plan(int64_t rows, int32_t heads, int32_t width, int32_t num_ctas, int
     pl.any_split = false;
     for (int64_t k = 1; k < c && !pl.any_split; ++k)
         if (cta_begin(pl.part, k) % width != 0) pl.any_split = true;
-    pl.max_pieces = static_cast<int>(std::min<int64_t>(max_pieces_bound(pl.part), 1 << 20));
+    pl.max_pieces = static_cast<int>(std::min<int64_t>(max_pieces_per_unit(pl.part), 1 << 20));
     pl.ws = ws_layout(rows, pl.groups, width, c);
     return pl;
 }

@@ -114,22 +114,24 @@ __host__ __device__ inline Segment cta_segment(const Partition& p, int64_t c, in
     return s;
 }
 
-// Bound on the CTAs sharing one unit: counted for up to 1024 units (CTAs with an empty
-// range inside a unit included); otherwise from the shortest CTA range, floor(T/C) slots,
-// which a unit of W slots meets at most ceil((W - 1) / floor(T/C)) + 1 times (up to C
-// times when ranges can be empty).
-inline int64_t max_pieces_bound(const Partition& p) {
+// Largest number of CTA ranges that one unit meets (CTAs with an empty range inside the
+// unit included, as the combine kernel walks them): pieces(u) = cta_of_slot(u*W + W - 1) -
+// cta_of_slot(u*W) + 1. A unit met by two or more ranges holds the start of one of them,
+// so the maximum is taken over the units where CTAs start, or over all units when there
+// are fewer units than CTAs.
+inline int64_t max_pieces_per_unit(const Partition& p) {
     const int64_t units = p.total_slots / p.width;
-    if (units <= 1024) {
-        int64_t mp = 1;
-        for (int64_t u = 0; u < units; ++u) {
-            const int64_t k = cta_of_slot(p, (u + 1) * p.width - 1) - cta_of_slot(p, u * p.width) + 1;
+    auto pieces = [&](int64_t u) { return cta_of_slot(p, u * p.width + p.width - 1) - cta_of_slot(p, u * p.width) + 1; };
+    int64_t mp = 1;
+    if (units <= p.ctas) {
+        for (int64_t u = 0; u < units; ++u) mp = pieces(u) > mp ? pieces(u) : mp;
+    } else {
+        for (int64_t c = 0; c < p.ctas; ++c) {
+            const int64_t k = pieces(cta_begin(p, c) / p.width);
             mp = k > mp ? k : mp;
         }
-        return mp;
     }
-    const int64_t min_range = p.total_slots / p.ctas;
-    return min_range > 0 ? (p.width - 1 + min_range - 1) / min_range + 1 : p.ctas;
+    return mp;
 }
 
 // ------------------------------------------------------------------------------------
@@ -193,7 +195,7 @@ cudaError_t launch_prologue(const PrologueParams& p, int blocks, bool programmat
 // tensor core better when it has much.
 cudaError_t launch_decode_64(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_decode_128(const DecodeParams& p, cudaStream_t stream);
-// max_pieces: an upper bound on the CTAs sharing one unit (selects the combine variant).
+// max_pieces: the most CTAs sharing one unit (max_pieces_per_unit; selects the variant).
 cudaError_t launch_combine(const CombineParams& p, int units, int max_pieces, cudaStream_t stream);
 cudaError_t decode_kernel_setup_64();
 cudaError_t decode_kernel_setup_128();

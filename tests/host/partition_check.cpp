@@ -1,8 +1,8 @@
 // Host-side checks of the static work partition in csrc/common.cuh (the helpers the decode
 // and combine kernels share): every (unit, slot) is covered by exactly one CTA segment, the
 // segment fields agree with the slot ranges, partial slots follow the first/last rule,
-// cta_of_slot inverts cta_begin, and max_pieces_bound never undercounts the CTAs sharing a
-// unit (and counts them exactly for up to 1024 units when no CTA range is empty).
+// cta_of_slot inverts cta_begin, and max_pieces_per_unit equals its per-unit definition
+// (which counts exactly the CTAs with slots in a unit when no CTA range is empty).
 // Exits non-zero on the first failure.
 #include <cstdio>
 #include <random>
@@ -62,10 +62,15 @@ int main() {
         for (size_t x = 0; x < covered.size(); ++x) CHECK(covered[x] == 1, "trial %d slot %zu", trial, x);
         int32_t mp = 1;
         for (int32_t k : ctas_in_unit) mp = k > mp ? k : mp;
-        CHECK(max_pieces_bound(p) >= mp, "trial %d bound %lld actual %d", trial,
-              static_cast<long long>(max_pieces_bound(p)), mp);
-        // Exact when no CTA range is empty (C <= T); empty ranges inside a unit are counted too.
-        if (units <= 1024 && C <= p.total_slots) CHECK(max_pieces_bound(p) == mp, "trial %d exact count", trial);
+        int64_t by_def = 1;  // the definition, unit by unit (empty CTA ranges counted)
+        for (int64_t u = 0; u < units; ++u) {
+            const int64_t k = cta_of_slot(p, u * W + W - 1) - cta_of_slot(p, u * W) + 1;
+            by_def = k > by_def ? k : by_def;
+        }
+        CHECK(max_pieces_per_unit(p) == by_def, "trial %d bound %lld definition %lld", trial,
+              static_cast<long long>(max_pieces_per_unit(p)), static_cast<long long>(by_def));
+        CHECK(by_def >= mp, "trial %d", trial);
+        if (C <= p.total_slots) CHECK(by_def == mp, "trial %d: no empty ranges, so every piece has slots", trial);
     }
     std::printf("partition ok\n");
     return 0;
