@@ -34,11 +34,13 @@ METRIC = "sparse MLA decode µs/step; effective HBM TB/s & % roofline (1×GB300)
 UNIT = "us/step"
 L2_BYTES = 129 * 1024 * 1024
 WORKLOADS = {"tiny": 0, "decode_batch": 1, "ragged": 2, "pooled_128k": 3, "verify_k4": 4}
-DEFAULT_WORKLOAD = "decode_batch"
+# The largest workload that fits one GPU (128 sequences x 128 heads over a 16M-token pool).
+DEFAULT_WORKLOAD = "pooled_128k"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# DRAM bytes (read + write) of one decode-kernel launch, from the ncu capture of the
-# current kernel summarised under profiles/ (decode_kernel_<workload>.md). A workload
-# absent here reports traffic null; an entry is removed whenever the kernel changes.
+# DRAM bytes (read + write) of one decode-kernel launch of each workload, as counted by
+# ncu (dram__bytes_read.sum + dram__bytes_write.sum) on the decode kernel as it is now. A
+# workload absent here reports traffic null; an entry is dropped whenever the decode
+# kernel changes, until it is counted again.
 MEASURED_TRAFFIC = {}
 
 
@@ -203,8 +205,8 @@ class ClockSampler:
 # the CUDA arm
 # ----------------------------------------------------------------------------------------
 
-def make_replicas(idx: int, seeds, device):
-    reps = [wl.config(idx, device=device, seed=wl.BASE_SEED + idx + 7919 * s) for s in seeds]
+def make_replicas(idx: int, seeds, device, num_seqs=None):
+    reps = [wl.config(idx, device=device, seed=wl.BASE_SEED + idx + 7919 * s, num_seqs=num_seqs) for s in seeds]
     return reps
 
 
@@ -221,7 +223,7 @@ def run_cuda(args, ws_n, rank, local):
     torch.cuda.set_device(device)
     idx = WORKLOADS[args.workload]
     n_rep = args.replicas or replica_count(idx)
-    reps = make_replicas(idx, shard_replicas(n_rep, ws_n, rank), device)
+    reps = make_replicas(idx, shard_replicas(n_rep, ws_n, rank), device, args.seqs or None)
     w0 = reps[0]
     cost = algorithmic_cost(w0)
     verify = w0.base_lens is not None
@@ -333,12 +335,7 @@ def run_cuda(args, ws_n, rank, local):
         "warmup": W, "ms_per_step": round(us_per_step / 1e3, 6), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
         "effective_tbs": round(ws_n * cost["bytes"] / (us_per_step * 1e-6) / 1e12, 4),
-        "config": {"workload": w0.name, "rows": w0.rows, "heads": w0.num_q_heads, "sel_width": w0.sel_width,
-                   "block_size": w0.block_size, "selected_tokens_per_step": cost["selected_tokens"],
-                   "algorithmic_bytes_per_step": cost["bytes"], "algorithmic_flops_per_step": cost["flops"],
-                   "l2": f"{n_rep} rotating input replicas per GPU, inputs of consecutive steps differ and "
-                         f"exceed L2 together", "graph_steps": g,
-                   "parallelism": f"replicas x{ws_n}" if ws_n > 1 else "1 GPU"},
+        "config": config_dict(w0, cost, n_rep, g, ws_n),
         "roofline": roof,
         "gpu_launches": K * launches_per_step,
         "clocks": clocks,
@@ -346,6 +343,16 @@ def run_cuda(args, ws_n, rank, local):
     }
     line["_w0"] = w0
     return line
+
+
+def config_dict(w: wl.Workload, cost: dict, n_rep: int, graph_steps: int, ws_n: int) -> dict:
+    """The workload description printed by both arms (identical keys and values)."""
+    return {"workload": w.name, "rows": w.rows, "heads": w.num_q_heads, "sel_width": w.sel_width,
+            "block_size": w.block_size, "selected_tokens_per_step": cost["selected_tokens"],
+            "algorithmic_bytes_per_step": cost["bytes"], "algorithmic_flops_per_step": cost["flops"],
+            "l2": f"{n_rep} rotating input replicas per GPU, inputs of consecutive steps differ and "
+                  f"exceed L2 together", "graph_steps": graph_steps,
+            "parallelism": f"replicas x{ws_n}" if ws_n > 1 else "1 GPU"}
 
 
 def needs_combine(api, w, ctas) -> bool:
@@ -360,7 +367,10 @@ def needs_combine(api, w, ctas) -> bool:
 
 def run_e2e(api, reps, args, device, ws_n):
     """Same metric through dsa_mla_decode_host: per step, H2D of q / block tables /
-    seq_lens / selection from pinned memory, the decode, D2H of the output."""
+    seq_lens / selection from pinned memory, the decode, D2H of the output. Consecutive
+    steps alternate between two streams, each with its own device workspace and host
+    buffers, so one step's copies overlap the other step's kernels, as a serving loop
+    with two requests in flight does."""
     n = min(len(reps), 8)
     w0 = reps[0]
     verify = w0.base_lens is not None
@@ -372,8 +382,9 @@ def run_e2e(api, reps, args, device, ws_n):
                          out=torch.empty(r.q.shape, dtype=torch.bfloat16).pin_memory(), dev=r))
     nb = api.host_workspace_bytes(w0.num_seqs, w0.rows_per_seq, w0.num_q_heads, w0.sel_width,
                                   w0.block_tables.shape[0], w0.max_blocks_per_seq, int(verify), args.ctas)
-    ws = torch.zeros(nb, dtype=torch.uint8, device=device)
-    stream = torch.cuda.Stream(device)
+    lanes = 2 if n >= 2 else 1
+    wss = [torch.zeros(nb, dtype=torch.uint8, device=device) for _ in range(lanes)]
+    streams = [torch.cuda.Stream(device) for _ in range(lanes)]
 
     def call(i):
         h = host[i % n]
@@ -381,25 +392,35 @@ def run_e2e(api, reps, args, device, ws_n):
         vc = r.k_cache if r.v_cache is None else r.v_cache
         api.decode_host(h["q"], r.k_cache, vc, h["bt"], r.max_blocks_per_seq, h["sl"], h["sel"], r.num_seqs,
                         r.rows_per_seq, r.num_q_heads, r.block_size, r.cache_stride_bytes, r.k_scale, r.v_scale,
-                        r.sm_scale, h["out"], ws, verify_rows=int(verify), num_ctas=args.ctas, stream=stream)
+                        r.sm_scale, h["out"], wss[i % lanes], verify_rows=int(verify), num_ctas=args.ctas,
+                        stream=streams[i % lanes])
 
     steps = max(1, min(args.steps, args.e2e_steps))
-    for i in range(3):
+    # a step's host buffers are reused n steps later, after its copies have completed
+    assert n >= lanes
+    for i in range(4):
         call(i)
-    stream.synchronize()
+    torch.cuda.synchronize(device)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    done = [torch.cuda.Event() for _ in range(lanes)]
     barrier(ws_n)
-    e0.record(stream)
+    e0.record(streams[0])
+    for s in streams[1:]:
+        s.wait_event(e0)
     for i in range(steps):
         call(i)
-    e1.record(stream)
-    stream.synchronize()
+    for k, s in enumerate(streams):
+        done[k].record(s)
+        streams[0].wait_event(done[k])
+    e1.record(streams[0])
+    streams[0].synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1), ws_n, device)
     h = host[0]
     h2d = sum(t.numel() * t.element_size() for t in (h["q"], h["bt"], h["sl"], h["sel"]))
     d2h = h["out"].numel() * 2
     return {"value": round(ms * 1e3 / steps, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "steps": steps, "api": "dsa_mla_decode_host"}
+            "d2h_bytes_per_step": int(d2h), "steps": steps,
+            "api": f"dsa_mla_decode_host, {lanes} streams alternating"}
 
 
 # ----------------------------------------------------------------------------------------
@@ -450,7 +471,10 @@ def cpu_baseline(w: wl.Workload, budget_s: float) -> dict:
 def run_reference(args, ws_n, rank):
     idx = WORKLOADS[args.workload]
     dev = "cuda" if (idx >= 2 and torch.cuda.is_available()) else "cpu"
-    full = wl.config(idx, device=dev)
+    full = wl.config(idx, device=dev, num_seqs=args.seqs or None)
+    cost = algorithmic_cost(full)
+    n_rep = args.replicas or replica_count(idx)
+    config = config_dict(full, cost, n_rep, min(args.steps, args.graph_steps), ws_n)
     w = cpu_sample_workload(full)
     scale = full.rows / w.rows
     budget = max(0.05, min(2.0, 90.0 / max(1, args.steps + args.warmup)))
@@ -470,8 +494,7 @@ def run_reference(args, ws_n, rank):
     return {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws_n, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(value / 1e3, 3), "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": full.name, "rows": full.rows, "heads": full.num_q_heads,
-                       "sel_width": full.sel_width},
+            "config": config,
             "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": threads, "kind": "oracle",
                              "sample": f"per step: whole decode rows timed for ~{budget:.2f} s and scaled to "
                                        f"the {full.rows}-row step ({rows_timed} rows over {args.steps} steps)"},
@@ -489,6 +512,9 @@ def main():
     ap.add_argument("--workload", choices=list(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--ctas", type=int, default=0, help="decode grid size (0 = library default)")
     ap.add_argument("--replicas", type=int, default=0)
+    ap.add_argument("--seqs", type=int, default=0,
+                    help="sequences per batch (0 = the workload's own count); smaller batches serve "
+                         "profiler captures of the same kernel")
     ap.add_argument("--graph-steps", type=int, default=256)
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
@@ -502,7 +528,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return 0
-        print(json.dumps(run_reference(args, 1, rank)))
+        print(json.dumps(run_reference(args, ws_n, rank)))
         return 0
 
     if not torch.cuda.is_available():

@@ -17,13 +17,13 @@
  *   out[r,h,:] = sum_{j in S_r} softmax_j(sm_scale * q[r,h,:].(k_scale*K_j)) (v_scale*V_j)
  *               and 0 when S_r is empty.
  * kv_lora_rank is fixed at 512 and there is one latent KV head with no rope section
- * (attend.rs, "NoPE, and why no common/ kernel would do"; DsaDecodePaging::validate).
+ * (attend.rs, module doc on the NoPE layout; DsaDecodePaging::validate).
  *
  * Conventions for every entry point:
  *  - Device pointers are caller-owned CUDA device memory on the current device; the
  *    library never frees or keeps them. "stream" is a cudaStream_t passed as void*.
- *  - Calls enqueue work on the stream and return without synchronising (attend.rs,
- *    decode_attention: "Enqueued on stream, not synchronised"), except where stated.
+ *  - Calls enqueue work on the stream and return without synchronising, as the pages'
+ *    launcher does (attend.rs, decode_attention), except where stated.
  *  - Arguments are checked on the host before anything is enqueued; an invalid call
  *    returns its status and writes nothing.
  *  - A missing or unloadable kernel is a hard error (DSA_ERR_NO_KERNEL), never a
@@ -31,8 +31,9 @@
  *  - Problems only visible on the device (a block-table entry that is negative or past
  *    max_blocks_per_seq, a pipeline wait that ran out of time) do not fault: the kernel
  *    skips the access and records the first such status in the workspace's status
- *    word, read back with dsa_read_device_status / dsa_last_device_status. The output
- *    of a call that recorded a device status is undefined.
+ *    word, read back with dsa_read_device_status / dsa_last_device_status /
+ *    dsa_static_device_status. The output of a call that recorded a device status is
+ *    undefined.
  */
 #ifndef DSA_MLA_H
 #define DSA_MLA_H
@@ -72,8 +73,9 @@ const char* dsa_status_string(int32_t status);
  *                     seq*rows_per_seq + i; absorbed queries in latent space (attend.rs,
  *                     DsaDecodeInputs::q). 16-byte aligned.
  *  k_cache, v_cache   E4M3 paged latent cache; page p starts at byte p*cache_stride_bytes.
- *                     K and V are normally the same buffer (attend.rs, DsaDecodeInputs:
- *                     "K and V are the same buffer"); distinct buffers are read separately.
+ *                     In NoPE MLA K and V are one buffer, passed twice (attend.rs,
+ *                     DsaDecodeInputs); distinct buffers are also accepted and read
+ *                     separately.
  *                     16-byte aligned, non-NULL.
  *  block_tables       int32 page ids; the table of sequence s starts at
  *                     block_tables + s*max_blocks_per_seq (max_blocks_per_seq = 0: every
@@ -88,8 +90,9 @@ const char* dsa_status_string(int32_t status);
  *  cache_stride_bytes bytes per page, >= block_size*512 and a multiple of 16
  *                     (block_size*512 for a dense pool: decode_k.rs, cache_stride_bytes).
  *  k_scale, v_scale   cache dequantisation scales (attend.rs, DsaDecodeInputs).
- *  sm_scale           score scale; the pages pass kv_lora_rank^-0.5 (attend.rs,
- *                     decode_attention, "the score scale is over the latent width").
+ *  sm_scale           score scale; the pages' launcher passes kv_lora_rank^-0.5, since
+ *                     the scores are formed over the 512-wide latent (attend.rs,
+ *                     decode_attention).
  *  out                bf16 [R, num_q_heads, 512], latent space. 16-byte aligned.
  *
  * Uses a library-owned workspace per device, grown on demand with cudaMalloc; growing
@@ -108,7 +111,8 @@ int32_t dsa_mla_decode(const void* q, const void* k_cache, const void* v_cache,
  * attend_rows). Arguments as dsa_mla_decode with rows_per_seq = k, except:
  *  seq_lens  int32 [num_seqs]: the sequence length seq_len before the k new tokens.
  *            Row i (0 <= i < k) of sequence s sits at position seq_len + i and sees
- *            positions < seq_lens[s] + i + 1 (decode_k.rs: "sl[row] = pos + 1").
+ *            positions < seq_lens[s] + i + 1: each row's visible length is its own
+ *            position plus one (decode_k.rs, decode_k).
  * All k rows of a sequence share its block table.
  */
 int32_t dsa_mla_decode_k(const void* q, const void* k_cache, const void* v_cache,
@@ -127,14 +131,40 @@ size_t dsa_mla_decode_workspace_bytes(int32_t num_seqs, int32_t rows_per_seq,
                                       int32_t num_q_heads, int32_t sel_width, int32_t num_ctas);
 
 /*
+ * Per-call options of dsa_mla_decode_ws (NULL = all defaults). Zero-initialise and set the
+ * fields you need; zero means "default" in every field. The source pages have no
+ * counterpart to these options: they choose between equivalent launch shapes or serve
+ * measurement and testing, and never change what is computed beyond floating-point
+ * rounding order.
+ *  num_ctas       decode grid size; 0 = default (the SM count, fewer for small problems).
+ *                 Must match the num_ctas the workspace was sized for.
+ *  tile_tokens    KV tokens per decode tile: 0 = automatic (64-token tiles when each
+ *                 decode CTA has at most 256 selected slots of work, 128 otherwise),
+ *                 64 or 128 = that size. Any other value is DSA_ERR_INVALID_ARGUMENT.
+ *  wait_limit_ns  time limit of every pipeline wait inside the decode kernel; 0 = the
+ *                 default of one second. A wait that runs out records DSA_ERR_TIMEOUT in
+ *                 the status word, stops the kernel's pipeline and leaves the output
+ *                 undefined; the kernel still drains its own copies and tensor-core work
+ *                 before it exits. A small limit is only useful to exercise that path.
+ *  ev_begin, ev_end  optional cudaEvent_t (as void*) recorded on the stream immediately
+ *                 before and after the main decode kernel (inside graph capture they
+ *                 become event-record nodes).
+ */
+typedef struct dsa_decode_options {
+    int32_t num_ctas;
+    int32_t tile_tokens;
+    uint64_t wait_limit_ns;
+    void* ev_begin;
+    void* ev_end;
+} dsa_decode_options;
+
+/*
  * dsa_mla_decode_ws: dsa_mla_decode / dsa_mla_decode_k with caller-owned workspace
  * (device memory, 256-byte aligned, >= dsa_mla_decode_workspace_bytes for the same
  * shape and num_ctas). Never allocates, so it can be captured into a CUDA graph.
  *  verify_rows   0: seq_lens is per row (dsa_mla_decode); 1: seq_lens is per sequence
  *                and rows follow the verify rule (dsa_mla_decode_k).
- *  num_ctas      decode grid size, 0 = default (the SM count, fewer for small problems).
- *  ev_begin, ev_end  optional cudaEvent_t (as void*, NULL = none) recorded on the stream
- *                immediately before and after the main decode kernel.
+ *  options       per-call options (see dsa_decode_options), or NULL.
  * The first 256 bytes of the workspace hold the device status word of the latest call.
  */
 int32_t dsa_mla_decode_ws(const void* q, const void* k_cache, const void* v_cache,
@@ -143,8 +173,8 @@ int32_t dsa_mla_decode_ws(const void* q, const void* k_cache, const void* v_cach
                           int32_t num_seqs, int32_t rows_per_seq, int32_t num_q_heads,
                           int32_t block_size, int64_t cache_stride_bytes, float k_scale,
                           float v_scale, float sm_scale, void* out, int32_t verify_rows,
-                          void* workspace, size_t workspace_bytes, int32_t num_ctas,
-                          void* ev_begin, void* ev_end, void* stream);
+                          void* workspace, size_t workspace_bytes,
+                          const dsa_decode_options* options, void* stream);
 
 /*
  * dsa_mla_decode_host: the same decode with the per-step inputs and the output in HOST
@@ -204,26 +234,16 @@ int32_t dsa_mla_decode_static(const void* q, const void* k_cache, const void* v_
                               float v_scale, float sm_scale, void* out, void* stream);
 
 /*
- * dsa_set_tile_tokens: KV tokens per decode tile for every later call in this process.
- *  tile_tokens  0 = automatic (the default): 64-token tiles when each decode CTA has at
- *               most 256 selected slots of work (small batches, where a shorter pipeline
- *               matters most), 128-token tiles otherwise (better tensor-core use);
- *               64 or 128 = that size for every call.
- * Results agree with either size to floating-point rounding order. Any other value
- * returns DSA_ERR_INVALID_ARGUMENT and changes nothing. Calls already enqueued, or
- * captured into a CUDA graph, keep the size they were launched with. Not thread-safe
- * against concurrent decode calls. The source pages have no counterpart to this call.
- */
-int32_t dsa_set_tile_tokens(int32_t tile_tokens);
-
-/*
  * Device status of the latest call on a caller workspace (dsa_mla_decode_ws /
- * dsa_mla_decode_host) or on the library workspace of the current device
- * (dsa_last_device_status). Synchronises the stream, writes the status to *status_out
- * and returns DSA_OK, or returns DSA_ERR_CUDA.
+ * dsa_mla_decode_host), on the library workspace of the current device
+ * (dsa_last_device_status), or on the fixed array of dsa_mla_decode_static
+ * (dsa_static_device_status; like that entry point it allocates nothing). Each
+ * synchronises the stream, writes the status to *status_out and returns DSA_OK, or
+ * returns DSA_ERR_CUDA.
  */
 int32_t dsa_read_device_status(const void* workspace, int32_t* status_out, void* stream);
 int32_t dsa_last_device_status(int32_t* status_out, void* stream);
+int32_t dsa_static_device_status(int32_t* status_out, void* stream);
 
 #ifdef __cplusplus
 }

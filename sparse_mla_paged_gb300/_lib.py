@@ -25,22 +25,30 @@ STATUS = {
 DSA_OK = 0
 
 _P, _I32, _I64, _F32, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+
+
+class DecodeOptions(ctypes.Structure):
+    """dsa_decode_options (include/dsa_mla.h)."""
+    _fields_ = [("num_ctas", ctypes.c_int32), ("tile_tokens", ctypes.c_int32), ("wait_limit_ns", ctypes.c_uint64),
+                ("ev_begin", ctypes.c_void_p), ("ev_end", ctypes.c_void_p)]
+
+
 _DECODE_ARGS = [_P, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I64, _F32, _F32, _F32, _P]
 SIGNATURES = {
     "dsa_abi_version": ([], _I32),
-    "dsa_set_tile_tokens": ([_I32], _I32),
     "dsa_status_string": ([_I32], ctypes.c_char_p),
     "dsa_mla_decode": (_DECODE_ARGS + [_P], _I32),
     "dsa_mla_decode_k": (_DECODE_ARGS + [_P], _I32),
     "dsa_mla_decode_static": (_DECODE_ARGS + [_P], _I32),
     "dsa_mla_decode_workspace_bytes": ([_I32, _I32, _I32, _I32, _I32], _SZ),
-    "dsa_mla_decode_ws": (_DECODE_ARGS + [_I32, _P, _SZ, _I32, _P, _P, _P], _I32),
+    "dsa_mla_decode_ws": (_DECODE_ARGS + [_I32, _P, _SZ, ctypes.POINTER(DecodeOptions), _P], _I32),
     "dsa_mla_decode_host_workspace_bytes": ([_I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32], _SZ),
     "dsa_mla_decode_host": ([_P, _P, _P, _P, _I32, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I64, _F32,
                              _F32, _F32, _P, _I32, _P, _SZ, _I32, _P], _I32),
     "dsa_resolve_indices": ([_P, _P, _I32, _I32, _P, _P, _P], _I32),
     "dsa_read_device_status": ([_P, _P, _P], _I32),
     "dsa_last_device_status": ([_P, _P], _I32),
+    "dsa_static_device_status": ([_P, _P], _I32),
 }
 
 _lock = threading.Lock()

@@ -35,11 +35,6 @@ def abi_version() -> int:
     return int(_lib.load().dsa_abi_version())
 
 
-def set_tile_tokens(tile_tokens: int) -> None:
-    """KV tokens per decode tile for later calls: 0 = automatic, 64 or 128 (dsa_set_tile_tokens)."""
-    _lib.check(_lib.load().dsa_set_tile_tokens(int(tile_tokens)), "dsa_set_tile_tokens")
-
-
 def status_string(status: int) -> str:
     return _lib.load().dsa_status_string(int(status)).decode()
 
@@ -96,18 +91,28 @@ def alloc_workspace(num_seqs, rows_per_seq, num_q_heads, sel_width, num_ctas=0, 
     return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
 
 
+def options(num_ctas=0, tile_tokens=0, wait_limit_ns=0, ev_begin=None, ev_end=None) -> "_lib.DecodeOptions":
+    """A dsa_decode_options struct (zero fields take the library defaults)."""
+    o = _lib.DecodeOptions()
+    o.num_ctas = int(num_ctas)
+    o.tile_tokens = int(tile_tokens)
+    o.wait_limit_ns = int(wait_limit_ns)
+    o.ev_begin = None if ev_begin is None else ev_begin.cuda_event
+    o.ev_end = None if ev_end is None else ev_end.cuda_event
+    return o
+
+
 def decode_ws(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, sel_indices, num_seqs,
               rows_per_seq, num_q_heads, block_size, cache_stride_bytes, k_scale, v_scale, sm_scale, out,
               workspace: torch.Tensor, verify_rows=0, num_ctas=0, ev_begin=None, ev_end=None,
-              stream=None) -> torch.Tensor:
-    """dsa_mla_decode_ws: caller workspace (capturable); optional events around the decode kernel."""
+              tile_tokens=0, wait_limit_ns=0, stream=None) -> torch.Tensor:
+    """dsa_mla_decode_ws: caller workspace (capturable) and per-call options."""
     a = _decode_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, sel_indices, num_seqs,
                      rows_per_seq, num_q_heads, block_size, cache_stride_bytes, k_scale, v_scale, sm_scale, out)
     _need(workspace, torch.uint8, "workspace")
-    e0 = None if ev_begin is None else ev_begin.cuda_event
-    e1 = None if ev_end is None else ev_end.cuda_event
-    check(_lib.load().dsa_mla_decode_ws(*a, int(verify_rows), _ptr(workspace), workspace.numel(), int(num_ctas),
-                                        e0, e1, _stream(stream)), "dsa_mla_decode_ws")
+    o = options(num_ctas, tile_tokens, wait_limit_ns, ev_begin, ev_end)
+    check(_lib.load().dsa_mla_decode_ws(*a, int(verify_rows), _ptr(workspace), workspace.numel(),
+                                        _lib.ctypes.byref(o), _stream(stream)), "dsa_mla_decode_ws")
     return out
 
 
@@ -162,6 +167,13 @@ def last_device_status(stream=None) -> int:
     return int(v.value)
 
 
+def static_device_status(stream=None) -> int:
+    """Device status word of the latest dsa_mla_decode_static call on the current device."""
+    v = _lib.ctypes.c_int32(0)
+    check(_lib.load().dsa_static_device_status(_lib.ctypes.byref(v), _stream(stream)), "dsa_static_device_status")
+    return int(v.value)
+
+
 # ----------------------------------------------------------------------------------------
 # Workload conveniences (a workloads.Workload holds the tensors and the scalars).
 # ----------------------------------------------------------------------------------------
@@ -172,13 +184,18 @@ def _workload_args(w):
 
 
 def decode_workload(w, out=None, workspace=None, num_ctas=0, verify=None, stream=None, ev_begin=None,
-                    ev_end=None) -> torch.Tensor:
+                    ev_end=None, tile_tokens=0, wait_limit_ns=0) -> torch.Tensor:
     """Run the decode on a Workload. verify=True uses the k-row entry point with the
-    workload's per-sequence base lengths."""
+    workload's per-sequence base lengths. Per-call options (num_ctas, tile_tokens,
+    wait_limit_ns, events) go through dsa_mla_decode_ws; without a workspace one is
+    allocated for the call."""
     q, kc, vc, bt, mbps = _workload_args(w)
     out = torch.empty_like(q) if out is None else out
     verify = (w.base_lens is not None) if verify is None else verify
     lens = w.base_lens if verify else w.seq_lens
+    if workspace is None and (num_ctas or tile_tokens or wait_limit_ns or ev_begin is not None):
+        workspace = alloc_workspace(w.num_seqs, w.rows_per_seq, w.num_q_heads, w.sel_width, num_ctas,
+                                    device=q.device)
     if workspace is None:
         fn = decode_k if verify else decode
         return fn(q, kc, vc, bt, mbps, lens, w.sel_indices, w.num_seqs, w.rows_per_seq, w.num_q_heads,
@@ -186,4 +203,4 @@ def decode_workload(w, out=None, workspace=None, num_ctas=0, verify=None, stream
     return decode_ws(q, kc, vc, bt, mbps, lens, w.sel_indices, w.num_seqs, w.rows_per_seq, w.num_q_heads,
                      w.block_size, w.cache_stride_bytes, w.k_scale, w.v_scale, w.sm_scale, out, workspace,
                      verify_rows=1 if verify else 0, num_ctas=num_ctas, ev_begin=ev_begin, ev_end=ev_end,
-                     stream=stream)
+                     tile_tokens=tile_tokens, wait_limit_ns=wait_limit_ns, stream=stream)

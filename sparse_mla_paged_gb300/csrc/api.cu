@@ -23,7 +23,6 @@ struct DeviceState {
 
 std::mutex g_mu;
 std::vector<DeviceState> g_devices;
-int32_t g_tile_tokens = 0;  // dsa_set_tile_tokens: 0 = automatic, else 64 or 128
 #ifdef DSA_TRACE
 unsigned long long* g_trace = nullptr;  // trace builds only: per-CTA decode timeline
 #endif
@@ -108,7 +107,33 @@ struct Plan {
     WsLayout ws;
 };
 
-Plan make_plan(int64_t rows, int32_t heads, int32_t width, int32_t num_ctas, int sms) {
+// Per-call choices (dsa_decode_options with its defaults filled in).
+struct CallOptions {
+    int32_t num_ctas = 0;
+    int32_t tile_tokens = 0;
+    uint64_t wait_limit_ns = 0;
+    cudaEvent_t ev0 = nullptr, ev1 = nullptr;
+};
+
+constexpr uint64_t kDefaultWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
+
+int32_t read_options(const dsa_decode_options* o, CallOptions* out) {
+    CallOptions c;
+    if (o) {
+        if (o->num_ctas < 0) return DSA_ERR_INVALID_ARGUMENT;
+        if (o->tile_tokens != 0 && o->tile_tokens != 64 && o->tile_tokens != 128) return DSA_ERR_INVALID_ARGUMENT;
+        c.num_ctas = o->num_ctas;
+        c.tile_tokens = o->tile_tokens;
+        c.wait_limit_ns = o->wait_limit_ns;
+        c.ev0 = static_cast<cudaEvent_t>(o->ev_begin);
+        c.ev1 = static_cast<cudaEvent_t>(o->ev_end);
+    }
+    if (c.wait_limit_ns == 0) c.wait_limit_ns = kDefaultWaitLimitNs;
+    *out = c;
+    return DSA_OK;
+}
+
+Plan make_plan(int64_t rows, int32_t heads, int32_t width, int32_t num_ctas, int sms, int32_t tile_tokens = 0) {
     Plan pl;
     pl.rows = rows;
     pl.groups = (heads + kHeadsPerCta - 1) / kHeadsPerCta;
@@ -123,7 +148,7 @@ Plan make_plan(int64_t rows, int32_t heads, int32_t width, int32_t num_ctas, int
         if (c < 1) c = 1;
     }
     pl.part.ctas = static_cast<int32_t>(c);
-    pl.small_tiles = g_tile_tokens == 0 ? pl.part.total_slots <= 2 * kCtaMinSlots * c : g_tile_tokens == 64;
+    pl.small_tiles = tile_tokens == 0 ? pl.part.total_slots <= 2 * kCtaMinSlots * c : tile_tokens == 64;
     pl.any_split = false;
     for (int64_t k = 1; k < c && !pl.any_split; ++k)
         if (cta_begin(pl.part, k) % width != 0) pl.any_split = true;
@@ -132,8 +157,8 @@ Plan make_plan(int64_t rows, int32_t heads, int32_t width, int32_t num_ctas, int
     return pl;
 }
 
-int32_t enqueue(const Args& a, const Plan& pl, uint8_t* ws, cudaEvent_t ev0, cudaEvent_t ev1,
-                cudaStream_t stream) {
+int32_t enqueue(const Args& a, const Plan& pl, uint8_t* ws, const CallOptions& opt, cudaStream_t stream) {
+    const cudaEvent_t ev0 = opt.ev0, ev1 = opt.ev1;
     PrologueParams pp{};
     pp.sel = a.sel;
     pp.seq_lens = a.seq_lens;
@@ -178,6 +203,7 @@ int32_t enqueue(const Args& a, const Plan& pl, uint8_t* ws, cudaEvent_t ev0, cud
     dp.kv_same = a.k_cache == a.v_cache ? 1 : 0;
     dp.v_scale = a.v_scale;
     dp.early_dependents = early ? 1 : 0;
+    dp.wait_limit_ns = opt.wait_limit_ns;
 #ifdef DSA_TRACE
     dp.trace = g_trace;
 #endif
@@ -208,17 +234,21 @@ int32_t enqueue(const Args& a, const Plan& pl, uint8_t* ws, cudaEvent_t ev0, cud
     return st;
 }
 
-int32_t run_ws(const Args& a, void* workspace, size_t workspace_bytes, int32_t num_ctas, cudaEvent_t ev0,
-               cudaEvent_t ev1, cudaStream_t stream) {
+int32_t run_ws(const Args& a, void* workspace, size_t workspace_bytes, const dsa_decode_options* options,
+               cudaStream_t stream) {
     int32_t st = check_args(a);
     if (st != DSA_OK) return st;
-    if (!workspace || !aligned(workspace, 256) || num_ctas < 0) return DSA_ERR_INVALID_ARGUMENT;
+    CallOptions opt;
+    st = read_options(options, &opt);
+    if (st != DSA_OK) return st;
+    if (!workspace || !aligned(workspace, 256)) return DSA_ERR_INVALID_ARGUMENT;
     DeviceState* d = nullptr;
     st = current_device(&d);
     if (st != DSA_OK) return st;
-    const Plan pl = make_plan(static_cast<int64_t>(a.num_seqs) * a.rows_per_seq, a.heads, a.width, num_ctas, d->sms);
+    const Plan pl = make_plan(static_cast<int64_t>(a.num_seqs) * a.rows_per_seq, a.heads, a.width, opt.num_ctas,
+                              d->sms, opt.tile_tokens);
     if (workspace_bytes < pl.ws.total) return DSA_ERR_WORKSPACE;
-    return enqueue(a, pl, static_cast<uint8_t*>(workspace), ev0, ev1, stream);
+    return enqueue(a, pl, static_cast<uint8_t*>(workspace), opt, stream);
 }
 
 int32_t run_lib(const Args& a, cudaStream_t stream) {
@@ -248,7 +278,9 @@ int32_t run_lib(const Args& a, cudaStream_t stream) {
         }
         ws = d->ws;
     }
-    return enqueue(a, pl, static_cast<uint8_t*>(ws), nullptr, nullptr, stream);
+    CallOptions opt;
+    read_options(nullptr, &opt);
+    return enqueue(a, pl, static_cast<uint8_t*>(ws), opt, stream);
 }
 
 Args make_args(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
@@ -285,13 +317,7 @@ extern "C" {
 void dsa_debug_set_trace(void* buffer) { g_trace = static_cast<unsigned long long*>(buffer); }
 #endif
 
-int32_t dsa_abi_version(void) { return 1; }
-
-int32_t dsa_set_tile_tokens(int32_t tile_tokens) {
-    if (tile_tokens != 0 && tile_tokens != 64 && tile_tokens != 128) return DSA_ERR_INVALID_ARGUMENT;
-    g_tile_tokens = tile_tokens;
-    return DSA_OK;
-}
+int32_t dsa_abi_version(void) { return 2; }
 
 const char* dsa_status_string(int32_t status) {
     switch (status) {
@@ -346,12 +372,11 @@ int32_t dsa_mla_decode_ws(const void* q, const void* k_cache, const void* v_cach
                           int32_t sel_width, int32_t num_seqs, int32_t rows_per_seq, int32_t num_q_heads,
                           int32_t block_size, int64_t cache_stride_bytes, float k_scale, float v_scale,
                           float sm_scale, void* out, int32_t verify_rows, void* workspace, size_t workspace_bytes,
-                          int32_t num_ctas, void* ev_begin, void* ev_end, void* stream) {
+                          const dsa_decode_options* options, void* stream) {
     return run_ws(make_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, sel_indices,
                             sel_width, num_seqs, rows_per_seq, num_q_heads, block_size, cache_stride_bytes,
                             k_scale, v_scale, sm_scale, out, verify_rows),
-                  workspace, workspace_bytes, num_ctas, static_cast<cudaEvent_t>(ev_begin),
-                  static_cast<cudaEvent_t>(ev_end), static_cast<cudaStream_t>(stream));
+                  workspace, workspace_bytes, options, static_cast<cudaStream_t>(stream));
 }
 
 namespace {
@@ -424,7 +449,9 @@ int32_t dsa_mla_decode_host(const void* q_host, const void* k_cache, const void*
                        reinterpret_cast<const int32_t*>(ws + hs.sel), sel_width, num_seqs, rows_per_seq,
                        num_q_heads, block_size, cache_stride_bytes, k_scale, v_scale, sm_scale, ws + hs.out,
                        verify_rows);
-    st = enqueue(a, pl, ws, nullptr, nullptr, s);
+    CallOptions opt;
+    read_options(nullptr, &opt);
+    st = enqueue(a, pl, ws, opt, s);
     if (st != DSA_OK) return st;
     if (cudaMemcpyAsync(out_host, ws + hs.out, qb, cudaMemcpyDeviceToHost, s) != cudaSuccess) return DSA_ERR_CUDA;
     return DSA_OK;

@@ -24,12 +24,18 @@ constexpr int kBitmapWords = 8192;     // resolve bitmap: seq_len up to 262144 t
 constexpr int kResolveThreads = 256;
 
 // Probabilities are carried as P' = 2^(x - m + kPBias) (x, m in log2 units) split into two
-// E4M3 terms. A head's reference max m is raised, to its tile max plus kRescaleSlack, only
-// when a tile's score exceeds m by more than kRescaleMargin; so P' stays below
-// 2^(kPBias + kRescaleMargin) < 448, the E4M3 maximum, and rescales are rare.
+// E4M3 terms. A head's reference m is reset to its tile max plus kRescaleSlack when the
+// tile max exceeds m by more than kRescaleMargin (so P' stays below
+// 2^(kPBias + kRescaleMargin) < 448, the E4M3 maximum) and also when the tile max falls
+// more than kRescaleDrop below m (so a tile far under an earlier maximum gets its own
+// exponent window instead of sinking into E4M3's subnormal range and below it). A
+// downward reset never takes m more than kRescaleFloor below the highest reference of the
+// head, which keeps the rescaled FP32 accumulator far from overflow.
 constexpr float kPBias = 7.0f;
 constexpr float kRescaleMargin = 1.75f;
-constexpr float kRescaleSlack = 3.0f;
+constexpr float kRescaleSlack = 1.0f;
+constexpr float kRescaleDrop = 8.0f;
+constexpr float kRescaleFloor = 64.0f;
 
 // Device status codes mirror dsa_status.
 constexpr int kStatusBounds = DSA_ERR_DEVICE_BOUNDS;
@@ -170,6 +176,7 @@ struct DecodeParams {
     int32_t kv_same;
     float v_scale;
     int32_t early_dependents;  // let the next kernel launch once every CTA has started
+    uint64_t wait_limit_ns;    // time limit of each pipeline wait (DSA_ERR_TIMEOUT past it)
     unsigned long long* trace;  // per-CTA timeline, used only by -DDSA_TRACE builds
 };
 

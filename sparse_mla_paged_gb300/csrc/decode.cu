@@ -147,7 +147,7 @@ __device__ __forceinline__ void fail(const DecodeParams& p, volatile int* abort_
 // reconverged before any warp-aligned tcgen05 or barrier instruction that follows.
 __device__ __forceinline__ void warp_wait(const DecodeParams& p, uint32_t bar, uint32_t parity,
                                           volatile int* abort_flag) {
-    if (!mbar_wait(bar, parity, abort_flag)) fail(p, abort_flag, kStatusTimeout);
+    if (!mbar_wait(bar, parity, abort_flag, p.wait_limit_ns)) fail(p, abort_flag, kStatusTimeout);
     __syncwarp();
 }
 
@@ -155,10 +155,11 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
     return f32x2_to_e4m3x2(a, b) | (f32x2_to_e4m3x2(c, d) << 16);
 }
 
-// Keeps sign, exponent and the top three mantissa bits (an E4M3-representable value for
-// magnitudes in E4M3's normal range).
+// x rounded to 4 significant bits (sign, exponent and the top three mantissa bits, round
+// half up on the magnitude): an E4M3-representable value for magnitudes in E4M3's normal
+// range, leaving a remainder of at most half a unit in its last place.
 __device__ __forceinline__ float hi_part(float x) {
-    return __uint_as_float(__float_as_uint(x) & 0xFFF00000u);
+    return __uint_as_float((__float_as_uint(x) + 0x00080000u) & 0xFFF00000u);
 }
 
 __device__ __forceinline__ void griddep_wait() {
@@ -282,7 +283,8 @@ __device__ __forceinline__ void mma_wait(const DecodeParams& p, uint32_t bar, ui
     for (;;) {
         mbar_try_wait_hint(bar, parity, kPollHintNs);
         if (warp_poll(bar, parity)) return;
-        const bool give_up = __shfl_sync(0xffffffffu, (*abort_flag != 0) || globaltimer_ns() - t0 > kWaitLimitNs, 0);
+        const bool give_up =
+            __shfl_sync(0xffffffffu, (*abort_flag != 0) || globaltimer_ns() - t0 > p.wait_limit_ns, 0);
         if (give_up) {
             fail(p, abort_flag, kStatusTimeout);
             return;
@@ -381,7 +383,7 @@ __device__ void run_mma(const DecodeParams& p, uint32_t sbase, uint32_t tmem, vo
                 }
                 if (!qk_done || !pv_done) {
                     const bool give_up =
-                        __shfl_sync(0xffffffffu, (*abort_flag != 0) || globaltimer_ns() - t_start > kWaitLimitNs, 0);
+                        __shfl_sync(0xffffffffu, (*abort_flag != 0) || globaltimer_ns() - t_start > p.wait_limit_ns, 0);
                     if (give_up) {
                         fail(p, abort_flag, kStatusTimeout);
                         break;
@@ -508,6 +510,7 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
         load_q(s.unit);
         const float c = p.qscale[static_cast<int64_t>(s.unit) * kHeadsPerCta + hq];
         float m_ref = kNegInf;  // reference max of head hq (log2 units)
+        float m_top = kNegInf;  // highest reference of head hq so far
         float l_part = 0.0f;    // this thread's share of the row sum of P'
 
         for (int t = 0; t < tl.ntiles; ++t, ++tau) {
@@ -530,67 +533,51 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
             // its half, the lo lane the last kScores.
             const int tok0 = t * kTileTokens + half * kHalfCols + term * kScores;
             float x[kScores];
-            bool over = false;
+            float hmax = kNegInf;
 #pragma unroll
             for (int j = 0; j < kScores; ++j) {
                 const float send = __uint_as_float(term ? v[j] : v[kScores + j]);
                 const float mine = __uint_as_float(term ? v[kScores + j] : v[j]);
                 const float other = __shfl_xor_sync(0xffffffffu, send, 1);
                 x[j] = (tok0 + j < tl.n) ? (mine + other) * c : kNegInf;
-                over |= x[j] > m_ref + kRescaleMargin;
+                hmax = fmaxf(hmax, x[j]);
             }
-            const bool any_over = named_bar_any<kBarSoftmax, kSoftmaxThreads>(over);
+            // Max of head hq over this warp's half of the tile.
+            hmax = fmaxf(hmax, __shfl_xor_sync(0xffffffffu, hmax, 1));
+            const bool over = hmax > m_ref + kRescaleMargin;
+            const bool under = hmax < m_ref - kRescaleDrop && m_ref > m_top - kRescaleFloor;
+            const bool any_change = named_bar_any<kBarSoftmax, kSoftmaxThreads>(over || under);
             if (st == 0 && (tau == 2 || tau == 3)) DSA_TRACE_AT(p, 73 + 8 * (tau - 2));
-            if (any_over) {
-                // Raise the reference max of every head whose tile max exceeds it by more
-                // than the margin; rescale O and the row sums by 2^(m_old - m_new).
-                float hmax = x[0];
-#pragma unroll
-                for (int j = 1; j < kScores; ++j) hmax = fmaxf(hmax, x[j]);
-                hmax = fmaxf(hmax, __shfl_xor_sync(0xffffffffu, hmax, 1));
+            // 32-head blocks of O^T that need rescaling before this tile's P.V (uniform).
+            bool resc[2] = {false, false};
+            if (any_change) {
+                // Reset the reference of every head whose tile max exceeds it by more than
+                // the margin, or lies more than kRescaleDrop below it; O and the row sums
+                // are rescaled by 2^(m_old - m_new).
                 if (term == 0) hm_s[half * kHeadsPerCta + hq] = hmax;
                 named_bar_sync<kBarSoftmax, kSoftmaxThreads>();
                 if (st == 0 && (tau == 2 || tau == 3)) DSA_TRACE_AT(p, 77 + 8 * (tau - 2));
                 const float tm = fmaxf(hm_s[hq], hm_s[kHeadsPerCta + hq]);
-                const float m_new = tm > m_ref + kRescaleMargin ? tm + kRescaleSlack : m_ref;
+                float m_new = m_ref;
+                if (tm > m_ref + kRescaleMargin || (tm < m_ref - kRescaleDrop && m_ref > m_top - kRescaleFloor))
+                    m_new = fmaxf(tm + kRescaleSlack, m_top - kRescaleFloor);
                 const float alpha = m_ref == kNegInf ? 0.0f : ex2_approx(m_ref - m_new);
                 l_part *= alpha;
                 m_ref = m_new;
+                m_top = fmaxf(m_top, m_new);
                 if (term == 0 && half == 0) alpha_s[hq] = alpha;
                 named_bar_sync<kBarSoftmax, kSoftmaxThreads>();
                 if (t > 0) {
                     // Blocks of 32 heads whose factors are all 1 are left alone.
-                    float bmin[2];
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
-                        float m = 1.0f;
+                        bool ch = false;
 #pragma unroll
                         for (int h = 0; h < 32; h += 4) {
                             const float4 a4 = *reinterpret_cast<const float4*>(alpha_s + hh * 32 + h);
-                            m = fminf(m, fminf(fminf(a4.x, a4.y), fminf(a4.z, a4.w)));
+                            ch |= (a4.x != 1.0f) | (a4.y != 1.0f) | (a4.z != 1.0f) | (a4.w != 1.0f);
                         }
-                        bmin[hh] = m;
-                    }
-                    if (fminf(bmin[0], bmin[1]) < 1.0f) {
-                        // O^T columns are heads: this warp rescales its lanes of chunks
-                        // 2*half and 2*half + 1, once the P.V before this tile is done.
-                        warp_wait(p, barp(BAR_PVDONE0 + ((tau - 1) & 1)), ((tau - 1) >> 1) & 1, abort_flag);
-                        tc_fence_after();
-#pragma unroll 1
-                        for (int mc2 = 0; mc2 < 2; ++mc2) {
-#pragma unroll 1
-                            for (int hh = 0; hh < 2; ++hh) {
-                                if (bmin[hh] >= 1.0f) continue;
-                                const uint32_t ta = tmem + lane_base + kTmemO + (2 * half + mc2) * 64 + hh * 32;
-                                uint32_t o[32];
-                                tmem_ld_x32(ta, o);
-#pragma unroll
-                                for (int k = 0; k < 32; ++k)
-                                    o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha_s[hh * 32 + k]);
-                                tmem_st_x32(ta, o);
-                            }
-                        }
-                        tmem_wait_st();
+                        resc[hh] = ch;
                     }
                 }
             }
@@ -623,6 +610,29 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
                 st_shared_v4(pb + kPTermBytes + p_off + c * 1024, lw[4 * c], lw[4 * c + 1], lw[4 * c + 2], lw[4 * c + 3]);
             }
             fence_proxy_async_smem();
+            if (resc[0] || resc[1]) {
+                // O^T columns are heads: this warp rescales its lanes of chunks 2*half and
+                // 2*half + 1 once the P.V before this tile is done. Doing it after the P
+                // write lets that P.V run while this tile's probabilities are formed; this
+                // tile's P.V waits for the rescale through the P-full barrier below.
+                warp_wait(p, barp(BAR_PVDONE0 + ((tau - 1) & 1)), ((tau - 1) >> 1) & 1, abort_flag);
+                tc_fence_after();
+#pragma unroll 1
+                for (int mc2 = 0; mc2 < 2; ++mc2) {
+#pragma unroll 1
+                    for (int hh = 0; hh < 2; ++hh) {
+                        if (!resc[hh]) continue;
+                        const uint32_t ta = tmem + lane_base + kTmemO + (2 * half + mc2) * 64 + hh * 32;
+                        uint32_t o[32];
+                        tmem_ld_x32(ta, o);
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha_s[hh * 32 + k]);
+                        tmem_st_x32(ta, o);
+                    }
+                }
+                tmem_wait_st();
+            }
             if (st == 0 && (tau == 2 || tau == 3)) DSA_TRACE_AT(p, 76 + 8 * (tau - 2));
             tc_fence_before();
             __syncwarp();
@@ -751,12 +761,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
         const uint32_t db = sbase + kOffBars + 8 * BAR_DRAIN;
         tc_commit_el(db, elect_one());
         uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(db, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+        while (!mbar_try_wait(db, 0) && globaltimer_ns() - t0 < kDrainLimitNs) {
         }
         DSA_TRACE_AT(p, 11);
         const uint32_t done = sbase + kOffBars + 8 * BAR_DONE;
         t0 = globaltimer_ns();
-        while (!mbar_try_wait(done, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+        while (!mbar_try_wait(done, 0) && globaltimer_ns() - t0 < kDrainLimitNs) {
         }
         __syncwarp();
     } else {

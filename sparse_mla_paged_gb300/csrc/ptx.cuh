@@ -1,9 +1,10 @@
 // Inline-PTX wrappers for sm_103a: mbarrier, cp.async, bulk copies, tcgen05 (TMEM
 // allocation, MMA, commit, TMEM loads/stores) and FP8 conversion.
 //
-// Every wait on an mbarrier is bounded: after kWaitLimitNs of %globaltimer time (or as
-// soon as the CTA's abort flag is raised) it gives up and reports failure, so that a
-// broken pipeline returns an error status instead of hanging the GPU.
+// Every wait on an mbarrier is bounded: after a limit of %globaltimer time (a kernel
+// parameter for the pipeline's waits, kDrainLimitNs for the final drain) or as soon as the
+// CTA's abort flag is raised, it gives up and reports failure, so that a broken pipeline
+// returns an error status instead of hanging the GPU.
 #pragma once
 
 #include <cstdint>
@@ -11,7 +12,9 @@
 
 namespace dsa {
 
-constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
+// Limit of the waits that drain a CTA's own asynchronous work before it frees tensor
+// memory and exits; independent of the pipeline's limit, so the drain is never cut short.
+constexpr uint64_t kDrainLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -50,20 +53,9 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity)
         : "memory");
     return ok;
 }
-// As mbar_try_wait, but the thread may stay suspended (not issuing) for up to
-// kSuspendHintNs while the phase is incomplete; it resumes as soon as the phase completes.
+// Longest time a waiting thread stays suspended (not issuing) in one try_wait while the
+// phase is incomplete; it resumes as soon as the phase completes.
 constexpr uint32_t kSuspendHintNs = 20000;
-__device__ __forceinline__ uint32_t mbar_try_wait_suspend(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
-        : "memory");
-    return ok;
-}
 // As mbar_try_wait, with the suspend hint given in nanoseconds.
 __device__ __forceinline__ uint32_t mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
     uint32_t ok;
@@ -78,14 +70,18 @@ __device__ __forceinline__ uint32_t mbar_try_wait_hint(uint32_t bar, uint32_t pa
 }
 constexpr uint32_t kPollHintNs = 500;
 // Waits for the phase with the given parity to complete. Returns false if the wait
-// ran out of time or the abort flag was raised meanwhile.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
+// ran out of time (limit_ns) or the abort flag was raised meanwhile.
+// The suspend hint never exceeds the limit, so a short limit is not hidden by a long
+// suspension that the phase happens to end.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort_flag,
+                                          uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
+    const uint32_t hint = limit_ns < kSuspendHintNs ? static_cast<uint32_t>(limit_ns) : kSuspendHintNs;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
-        if (mbar_try_wait_suspend(bar, parity)) return true;
+        if (mbar_try_wait_hint(bar, parity, hint)) return true;
         if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
 

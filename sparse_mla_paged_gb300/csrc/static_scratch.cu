@@ -60,5 +60,15 @@ extern "C" int32_t dsa_mla_decode_static(const void* q, const void* k_cache, con
     return dsa_mla_decode_ws(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, sel_indices,
                              sel_width, num_seqs, rows_per_seq, num_q_heads, block_size, cache_stride_bytes,
                              k_scale, v_scale, sm_scale, out, /*verify_rows=*/0, scratch, DSA_STATIC_SCRATCH_BYTES,
-                             /*num_ctas=*/0, nullptr, nullptr, stream);
+                             /*options=*/nullptr, stream);
+}
+
+// The status word of the latest static call is the first word of g_scratch; reading it
+// back is a copy from the looked-up device address into the caller's variable.
+extern "C" int32_t dsa_static_device_status(int32_t* status_out, void* stream) {
+    if (!status_out) return DSA_ERR_INVALID_ARGUMENT;
+    void* scratch = nullptr;
+    const int32_t st = scratch_address(&scratch);
+    if (st != DSA_OK) return st;
+    return dsa_read_device_status(scratch, status_out, stream);
 }

@@ -175,11 +175,12 @@ def tiny(device="cpu", seed: Optional[int] = None) -> Workload:
                     1, 1, H, bs, bs * LATENT, L // bs, 0.05, 0.05, 1.0 / 16.0)
 
 
-def decode_batch(device="cpu", seed: Optional[int] = None) -> Workload:
+def decode_batch(device="cpu", seed: Optional[int] = None, num_seqs: Optional[int] = None) -> Workload:
     """8 sequences x 64 heads, seq_len 4096, block_size 64 over a randomly permuted
-    512-page pool, sel_width 2048 = 2007 distinct ids + 41 holes (2%)."""
+    512-page pool, sel_width 2048 = 2007 distinct ids + 41 holes (2%). num_seqs draws a
+    smaller (or larger) batch of the same kind."""
     g = _gen(device, BASE_SEED + 1 if seed is None else seed)
-    S, H, L, bs, W = 8, 64, 4096, 64, 2048
+    S, H, L, bs, W = num_seqs or 8, 64, 4096, 64, 2048
     q = _q(S, H, 1.0, device, g)
     pages_per_seq = L // bs
     cache = _cache(S * pages_per_seq, bs * LATENT, "normal", 0.05, device, g)
@@ -190,18 +191,19 @@ def decode_batch(device="cpu", seed: Optional[int] = None) -> Workload:
         holes = torch.full((41,), -1, dtype=torch.int64, device=device)
         rows.append(_shuffle(torch.cat([ids, holes]), device, g))
     sel = torch.stack(rows).to(torch.int32)
-    return Workload("decode batch: 8 seqs x 64 heads, seq_len 4096, sel_width 2048", q, cache,
+    return Workload(f"decode batch: {S} seqs x 64 heads, seq_len 4096, sel_width 2048", q, cache,
                     None, bt, torch.full((S,), L, dtype=torch.int32, device=device), sel,
                     S, 1, H, bs, bs * LATENT, pages_per_seq, 0.05, 0.05, 1.0 / math.sqrt(512))
 
 
-def ragged(device="cpu", seed: Optional[int] = None) -> Workload:
+def ragged(device="cpu", seed: Optional[int] = None, num_seqs: Optional[int] = None) -> Workload:
     """64 sequences x 64 heads, seq_len uniform in [8192, 32768], block_size 64, pages
     scattered over a 2M-token pool; sel_width 2048 = 1536 distinct ids from
     [0, L-512) + 512 distinct from the last 512 positions; rows shorter than 2048
-    tokens would take every position and pad with holes."""
+    tokens would take every position and pad with holes. num_seqs draws a smaller batch
+    of the same kind."""
     g = _gen(device, BASE_SEED + 2 if seed is None else seed)
-    S, H, bs, W, pool_pages = 64, 64, 64, 2048, (2 << 20) // 64
+    S, H, bs, W, pool_pages = num_seqs or 64, 64, 64, 2048, (2 << 20) // 64
     lens = torch.randint(8192, 32768 + 1, (S,), generator=g, device=device)
     q = _q(S, H, 1.0, device, g)
     cache = _cache(pool_pages, bs * LATENT, "normal", 0.05, device, g)
@@ -224,17 +226,18 @@ def ragged(device="cpu", seed: Optional[int] = None) -> Workload:
                              _distinct(L - 512, L, 512, device, g)])
         rows.append(_shuffle(ids, device, g))
     sel = torch.stack(rows).to(torch.int32)
-    return Workload("ragged long-context: 64 seqs x 64 heads, seq_len U[8192,32768], sel_width 2048",
+    return Workload(f"ragged long-context: {S} seqs x 64 heads, seq_len U[8192,32768], sel_width 2048",
                     q, cache, None, bt, lens.to(torch.int32), sel, S, 1, H, bs, bs * LATENT, mbps,
                     0.05, 0.05, 1.0 / math.sqrt(512))
 
 
-def pooled_128k(device="cpu", seed: Optional[int] = None) -> Workload:
+def pooled_128k(device="cpu", seed: Optional[int] = None, num_seqs: Optional[int] = None) -> Workload:
     """128 sequences x 128 heads, seq_len 131072, block_size 64 (2048 pages each over a
     262144-page pool), index_kpool 4: 512 random distinct pools of 4 consecutive tokens
-    (sel_width 2048); q ~ N(0, 2^2); cache from Student-t(3) before quantisation."""
+    (sel_width 2048); q ~ N(0, 2^2); cache from Student-t(3) before quantisation.
+    num_seqs draws a smaller batch of the same kind (with its own pool)."""
     g = _gen(device, BASE_SEED + 3 if seed is None else seed)
-    S, H, L, bs, kpool, npools = 128, 128, 131072, 64, 4, 512
+    S, H, L, bs, kpool, npools = num_seqs or 128, 128, 131072, 64, 4, 512
     q = _q(S, H, 2.0, device, g)
     pps = L // bs
     cache = _cache(S * pps, bs * LATENT, "t3", 0.05, device, g)
@@ -244,18 +247,19 @@ def pooled_128k(device="cpu", seed: Optional[int] = None) -> Workload:
         pools = _distinct(0, L // kpool, npools, device, g)
         rows.append((pools[:, None] * kpool + torch.arange(kpool, device=device)[None, :]).reshape(-1))
     sel = torch.stack(rows).to(torch.int32)
-    return Workload("pooled selection at 128K: 128 seqs x 128 heads, 512 pools of 4", q, cache,
+    return Workload(f"pooled selection at 128K: {S} seqs x 128 heads, 512 pools of 4", q, cache,
                     None, bt, torch.full((S,), L, dtype=torch.int32, device=device), sel,
                     S, 1, H, bs, bs * LATENT, pps, 0.05, 0.05, 1.0 / math.sqrt(512),
                     meta={"index_kpool": kpool})
 
 
-def verify_k4(device="cpu", seed: Optional[int] = None) -> Workload:
+def verify_k4(device="cpu", seed: Optional[int] = None, num_seqs: Optional[int] = None) -> Workload:
     """32 sequences x k=4 consecutive verify rows (128 rows), 64 heads, base seq_len
     16384; row r sees positions < 16384 + r + 1; per row 2048 ids = 1536 shared by the
-    sequence's rows + 512 row-specific; block_size 64 over a permuted pool."""
+    sequence's rows + 512 row-specific; block_size 64 over a permuted pool. num_seqs
+    draws a smaller batch of the same kind."""
     g = _gen(device, BASE_SEED + 4 if seed is None else seed)
-    S, k, H, base, bs, W, shared = 32, 4, 64, 16384, 64, 2048, 1536
+    S, k, H, base, bs, W, shared = num_seqs or 32, 4, 64, 16384, 64, 2048, 1536
     q = _q(S * k, H, 1.0, device, g)
     pps = (base + k + bs - 1) // bs
     cache = _cache(S * pps, bs * LATENT, "normal", 0.05, device, g)
@@ -273,7 +277,7 @@ def verify_k4(device="cpu", seed: Optional[int] = None) -> Workload:
             own = free[_perm(free.numel(), device, g)[:W - shared]]
             rows.append(_shuffle(torch.cat([common, own]), device, g))
     sel = torch.stack(rows).to(torch.int32)
-    return Workload("multi-row verify: 32 seqs x k=4 rows x 64 heads, base seq_len 16384", q, cache,
+    return Workload(f"multi-row verify: {S} seqs x k=4 rows x 64 heads, base seq_len 16384", q, cache,
                     None, bt, lens.reshape(-1).to(torch.int32), sel, S, k, H, bs, bs * LATENT, pps,
                     0.05, 0.05, 1.0 / math.sqrt(512), base_lens=base_lens)
 
@@ -281,8 +285,12 @@ def verify_k4(device="cpu", seed: Optional[int] = None) -> Workload:
 CONFIGS = [tiny, decode_batch, ragged, pooled_128k, verify_k4]
 
 
-def config(index: int, device="cpu", seed: Optional[int] = None) -> Workload:
-    return CONFIGS[index](device=device, seed=seed)
+def config(index: int, device="cpu", seed: Optional[int] = None, num_seqs: Optional[int] = None) -> Workload:
+    if num_seqs is None:
+        return CONFIGS[index](device=device, seed=seed)
+    if index == 0:
+        raise ValueError("the tiny workload has one sequence")
+    return CONFIGS[index](device=device, seed=seed, num_seqs=num_seqs)
 
 
 # ------------------------------------------------------------------------------------
@@ -329,3 +337,46 @@ def random_case(*, num_seqs=1, rows_per_seq=1, heads=4, seq_len=256, block_size=
     return Workload(f"random case seed {seed}", q, kc, vc, bt, lens, sel, num_seqs, rows_per_seq,
                     heads, block_size, stride, 0 if shared_table else mbps, k_scale, v_scale,
                     (1.0 / math.sqrt(LATENT)) if sm_scale is None else sm_scale)
+
+
+def flat_tail(*, heads=64, width=2048, tail_value=20.0, dominant_at=("first", "middle", "last"),
+              gap_lo=4.0, gap_hi=24.0, device="cpu", seed=31337) -> Workload:
+    """One sequence per entry of `dominant_at`, each selecting `width` tokens: one dominant
+    token (the lowest, a middle or the highest selected id) and width - 1 tokens whose
+    cache rows are byte-identical (a flat tail of equal scores). The scores are set by
+    dimension 0 alone: q[h, 0] = gap_h, with gap_h swept from gap_lo to gap_hi over the
+    heads, the dominant row holds 448 there and the tail rows 0; with k_scale = 1/448 and
+    sm_scale = ln 2 the dominant score sits gap_h log2 units above the tail. The tail rows
+    hold `tail_value` (an E4M3 code) in every other dimension; the dominant row holds, in a
+    block of 7 dimensions per head, the code that nearly cancels that head's tail, so the
+    reference output there is close to zero and the absolute tolerance term decides."""
+    g = _gen(device, seed)
+    S, bs = len(dominant_at), 64
+    pages = (width + bs - 1) // bs
+    gaps = torch.linspace(gap_lo, gap_hi, heads, device=device, dtype=torch.float64)
+    q = torch.zeros((S, heads, LATENT), dtype=torch.float32, device=device)
+    q[:, :, 0] = gaps.to(torch.float32)
+    q = q.to(torch.bfloat16)
+    gq = q[0, :, 0].to(torch.float64)                      # the BF16 gaps actually used
+    tail = torch.full((LATENT,), tail_value, dtype=torch.float32, device=device)
+    tail[0] = 0.0
+    dom = torch.zeros((LATENT,), dtype=torch.float32, device=device)
+    dom[0] = 448.0
+    for h in range(min(heads, (LATENT - 1) // 7)):
+        share = (width - 1) * torch.exp2(-gq[h])         # tail weight over the dominant's
+        dom[1 + 7 * h:8 + 7 * h] = float(-tail_value * share.clamp(max=448.0 / max(tail_value, 1e-30)))
+    tail_b = tail.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+    dom_b = dom.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+    num_pages = S * pages
+    cache = tail_b.repeat(num_pages * bs).reshape(num_pages, bs * LATENT).clone()
+    bt = _perm(num_pages, device, g).to(torch.int32).reshape(S, pages)
+    rows = []
+    for s, where in enumerate(dominant_at):
+        d = {"first": 0, "middle": width // 2 - 7, "last": width - 1}[where]
+        page = int(bt[s, d // bs].item())
+        cache[page, (d % bs) * LATENT:(d % bs + 1) * LATENT] = dom_b
+        rows.append(_shuffle(torch.arange(width, device=device), device, g))
+    sel = torch.stack(rows).to(torch.int32)
+    return Workload(f"flat tail: {S} seqs x {heads} heads, width {width}, gaps {gap_lo}..{gap_hi}", q, cache,
+                    None, bt, torch.full((S,), width, dtype=torch.int32, device=device), sel, S, 1, heads, bs,
+                    bs * LATENT, pages, 1.0 / 448.0, 0.05, math.log(2.0))

@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    assert lib.dsa_abi_version() == 1
+    assert lib.dsa_abi_version() == 2
     for code, name in _lib.STATUS.items():
         s = lib.dsa_status_string(code).decode()
         assert s and s != "unknown status", name
@@ -68,14 +68,35 @@ def test_invalid_arguments_rejected_on_host(lib, over, code):
     assert _call(lib, **over) == code
 
 
-def test_decode_ws_rejects_bad_workspace_on_host(lib):
+def _ws_args():
     a = BASE
-    args = [a["q"], a["k"], a["v"], a["bt"], a["mbps"], a["sl"], a["sel"], a["width"], a["seqs"], a["rps"],
+    return [a["q"], a["k"], a["v"], a["bt"], a["mbps"], a["sl"], a["sel"], a["width"], a["seqs"], a["rps"],
             a["heads"], a["bs"], a["stride"], a["ks"], a["vs"], a["sm"], a["out"]]
-    assert lib.dsa_mla_decode_ws(*args, 0, None, 1 << 20, 0, None, None, None) == 1       # null workspace
-    assert lib.dsa_mla_decode_ws(*args, 0, 0x70010, 1 << 20, 0, None, None, None) == 1    # misaligned
-    assert lib.dsa_mla_decode_ws(*args, 2, 0x70000, 1 << 20, 0, None, None, None) == 1    # bad verify flag
-    assert lib.dsa_mla_decode_ws(*args, 0, 0x70000, 1 << 20, -1, None, None, None) == 1   # bad grid
+
+
+def test_decode_ws_rejects_bad_workspace_on_host(lib):
+    args = _ws_args()
+    assert lib.dsa_mla_decode_ws(*args, 0, None, 1 << 20, None, None) == 1       # null workspace
+    assert lib.dsa_mla_decode_ws(*args, 0, 0x70010, 1 << 20, None, None) == 1    # misaligned
+    assert lib.dsa_mla_decode_ws(*args, 2, 0x70000, 1 << 20, None, None) == 1    # bad verify flag
+
+
+@pytest.mark.parametrize("field,value", [("num_ctas", -1), ("tile_tokens", -1), ("tile_tokens", 1),
+                                         ("tile_tokens", 32), ("tile_tokens", 96), ("tile_tokens", 256)])
+def test_decode_ws_rejects_bad_options_on_host(lib, field, value):
+    o = _lib.DecodeOptions()
+    setattr(o, field, value)
+    assert lib.dsa_mla_decode_ws(*_ws_args(), 0, 0x70000, 1 << 20, ctypes.byref(o), None) == 1
+
+
+def test_options_struct_matches_the_header():
+    """The binding's struct has the header's fields, in order, with C layout."""
+    text = open(_lib.HEADER).read()
+    body = re.search(r"typedef struct dsa_decode_options \{(.*?)\} dsa_decode_options;", text, re.S).group(1)
+    fields = re.findall(r"(\w+)\s*;", body)
+    assert fields == [f for f, _ in _lib.DecodeOptions._fields_]
+    assert ctypes.sizeof(_lib.DecodeOptions) == 32
+    assert _lib.DecodeOptions.wait_limit_ns.offset == 8 and _lib.DecodeOptions.ev_begin.offset == 16
 
 
 def test_resolve_rejects_bad_arguments_on_host(lib):
@@ -98,9 +119,3 @@ def test_workspace_size_grows_with_the_problem(lib):
     assert base >= rows * width * (4 + 8) + rows * 4 + rows * 65536 + 2 * ctas * 64 * 512 * 2
     assert f(0, 1, 64, 2048, 152) == 0
 
-
-def test_tile_tokens_knob_checks_its_argument(lib):
-    for bad in (-1, 1, 32, 96, 256):
-        assert lib.dsa_set_tile_tokens(bad) == 1
-    for good in (64, 128, 0):
-        assert lib.dsa_set_tile_tokens(good) == 0

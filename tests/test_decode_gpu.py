@@ -113,11 +113,8 @@ def test_decode_cases(api, name):
                                   "multi seq", "rows per seq", "heavy tails", "negative score scale"])
 def test_decode_cases_forced_tile(api, name, tile):
     """Both builds of the decode kernel (64- and 128-token tiles) on the same inputs."""
-    api.set_tile_tokens(tile)
-    try:
-        _check(api, wl.random_case(seed=zlib.crc32(name.encode()) % 100000, **CASES[name]), f"{name} tile {tile}")
-    finally:
-        api.set_tile_tokens(0)
+    w = wl.random_case(seed=zlib.crc32(name.encode()) % 100000, **CASES[name])
+    _check(api, w, f"{name} tile {tile}", tile_tokens=tile, status_ok=False)
 
 
 @pytest.mark.parametrize("ctas", [1, 2, 3, 5, 17, 64, 152, 400])
@@ -313,3 +310,47 @@ def test_full_size_configs_sampled(api, cfg):
     ref = oracle.decode_workload(sub)
     assert_parity(out[rows], ref, f"config {cfg} sampled sequences {FULL[cfg]}")
     assert torch.isfinite(out.float()).all()
+
+
+# ------------------------------------------------------------------------------------
+# Flat tails: one dominant token and width - 1 tokens with identical scores far below it.
+# The probability operand has a finite exponent range; each decode tile must keep the
+# tail's weight whatever the gap (4 to 24 log2 units over the heads), wherever the
+# dominant token sits (first, middle, last) and however the row is split across CTAs.
+# ------------------------------------------------------------------------------------
+
+_FLAT = {}
+
+
+def _flat(tail_value):
+    if tail_value not in _FLAT:
+        w = wl.flat_tail(tail_value=tail_value)
+        _FLAT[tail_value] = (w, oracle.decode_workload(w))
+    return _FLAT[tail_value]
+
+
+@pytest.mark.parametrize("tail_value", [20.0, 80.0])
+@pytest.mark.parametrize("tile", [64, 128])
+@pytest.mark.parametrize("ctas", [0, 1, 3, 7])
+def test_flat_tail(api, tail_value, tile, ctas):
+    w, ref = _flat(tail_value)
+    out = _run(api, w, tile_tokens=tile, num_ctas=ctas)
+    assert_parity(out, ref, f"flat tail |v| {tail_value * w.v_scale} tile {tile} ctas {ctas}")
+
+
+# ------------------------------------------------------------------------------------
+# The bounded-wait path: a 1 ns wait limit makes the pipeline give up; the call records
+# DSA_ERR_TIMEOUT, drains and exits, and the next call on the same workspace is clean.
+# ------------------------------------------------------------------------------------
+
+def test_wait_timeout_sets_device_status_and_recovers(api):
+    w = wl.random_case(num_seqs=2, heads=64, seq_len=3000, sel_width=1024, seed=21)
+    wc = w.to("cuda")
+    ws = api.alloc_workspace(2, 1, 64, 1024)
+    api.decode_workload(wc, workspace=ws, wait_limit_ns=1)
+    torch.cuda.synchronize()
+    assert api.read_device_status(ws) == 7         # DSA_ERR_TIMEOUT
+    out = api.decode_workload(wc, workspace=ws)
+    torch.cuda.synchronize()
+    assert api.read_device_status(ws) == 0
+    assert_parity(out, oracle.decode_workload(w), "after a timed-out call")
