@@ -235,7 +235,7 @@ def run_cuda(args, ws_n, rank, local):
     def step(i, s, ev0=None, ev1=None):
         r = reps[i % n_rep]
         api.decode_workload(r, out=outs[i % n_rep], workspace=ws, num_ctas=args.ctas, verify=verify,
-                            stream=s, ev_begin=ev0, ev_end=ev1)
+                            stream=s, ev_begin=ev0, ev_end=ev1, tile_tokens=args.tile, gather_mode=args.gather_mode)
 
     # warm-up, eager
     with torch.cuda.stream(stream):
@@ -511,6 +511,10 @@ def main():
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
     ap.add_argument("--workload", choices=list(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--ctas", type=int, default=0, help="decode grid size (0 = library default)")
+    ap.add_argument("--tile", type=int, default=0, choices=[0, 64, 128],
+                    help="decode tile in tokens (0 = library default)")
+    ap.add_argument("--gather-mode", type=int, default=0, choices=[0, 1],
+                    help="0 = library default (tensor-map gathers on dense pages), 1 = per-thread copies")
     ap.add_argument("--replicas", type=int, default=0)
     ap.add_argument("--seqs", type=int, default=0,
                     help="sequences per batch (0 = the workload's own count); smaller batches serve "

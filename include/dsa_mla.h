@@ -141,11 +141,18 @@ size_t dsa_mla_decode_workspace_bytes(int32_t num_seqs, int32_t rows_per_seq,
  *  tile_tokens    KV tokens per decode tile: 0 = automatic (64-token tiles when each
  *                 decode CTA has at most 256 selected slots of work, 128 otherwise),
  *                 64 or 128 = that size. Any other value is DSA_ERR_INVALID_ARGUMENT.
+ *  gather_mode    how the decode fetches cache rows: 0 = automatic (tensor-map gathers
+ *                 when the pages are dense, cache_stride_bytes = block_size*512, and the
+ *                 caches are 128-byte aligned; per-thread 16-byte copies otherwise),
+ *                 1 = per-thread copies always. Any other value is
+ *                 DSA_ERR_INVALID_ARGUMENT.
  *  wait_limit_ns  time limit of every pipeline wait inside the decode kernel; 0 = the
  *                 default of one second. A wait that runs out records DSA_ERR_TIMEOUT in
  *                 the status word, stops the kernel's pipeline and leaves the output
  *                 undefined; the kernel still drains its own copies and tensor-core work
- *                 before it exits. A small limit is only useful to exercise that path.
+ *                 before it exits. A small limit is only useful to exercise that path;
+ *                 a limit below 500 ns makes every wait that is not already complete
+ *                 when first checked give up at once.
  *  ev_begin, ev_end  optional cudaEvent_t (as void*) recorded on the stream immediately
  *                 before and after the main decode kernel (inside graph capture they
  *                 become event-record nodes).
@@ -153,6 +160,8 @@ size_t dsa_mla_decode_workspace_bytes(int32_t num_seqs, int32_t rows_per_seq,
 typedef struct dsa_decode_options {
     int32_t num_ctas;
     int32_t tile_tokens;
+    int32_t gather_mode;
+    int32_t reserved; /* must be 0 */
     uint64_t wait_limit_ns;
     void* ev_begin;
     void* ev_end;

@@ -29,7 +29,8 @@ _P, _I32, _I64, _F32, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, cty
 
 class DecodeOptions(ctypes.Structure):
     """dsa_decode_options (include/dsa_mla.h)."""
-    _fields_ = [("num_ctas", ctypes.c_int32), ("tile_tokens", ctypes.c_int32), ("wait_limit_ns", ctypes.c_uint64),
+    _fields_ = [("num_ctas", ctypes.c_int32), ("tile_tokens", ctypes.c_int32), ("gather_mode", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("wait_limit_ns", ctypes.c_uint64),
                 ("ev_begin", ctypes.c_void_p), ("ev_end", ctypes.c_void_p)]
 
 

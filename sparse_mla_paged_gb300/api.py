@@ -91,11 +91,13 @@ def alloc_workspace(num_seqs, rows_per_seq, num_q_heads, sel_width, num_ctas=0, 
     return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
 
 
-def options(num_ctas=0, tile_tokens=0, wait_limit_ns=0, ev_begin=None, ev_end=None) -> "_lib.DecodeOptions":
+def options(num_ctas=0, tile_tokens=0, wait_limit_ns=0, ev_begin=None, ev_end=None,
+            gather_mode=0) -> "_lib.DecodeOptions":
     """A dsa_decode_options struct (zero fields take the library defaults)."""
     o = _lib.DecodeOptions()
     o.num_ctas = int(num_ctas)
     o.tile_tokens = int(tile_tokens)
+    o.gather_mode = int(gather_mode)
     o.wait_limit_ns = int(wait_limit_ns)
     o.ev_begin = None if ev_begin is None else ev_begin.cuda_event
     o.ev_end = None if ev_end is None else ev_end.cuda_event
@@ -105,12 +107,12 @@ def options(num_ctas=0, tile_tokens=0, wait_limit_ns=0, ev_begin=None, ev_end=No
 def decode_ws(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, sel_indices, num_seqs,
               rows_per_seq, num_q_heads, block_size, cache_stride_bytes, k_scale, v_scale, sm_scale, out,
               workspace: torch.Tensor, verify_rows=0, num_ctas=0, ev_begin=None, ev_end=None,
-              tile_tokens=0, wait_limit_ns=0, stream=None) -> torch.Tensor:
+              tile_tokens=0, wait_limit_ns=0, gather_mode=0, stream=None) -> torch.Tensor:
     """dsa_mla_decode_ws: caller workspace (capturable) and per-call options."""
     a = _decode_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, sel_indices, num_seqs,
                      rows_per_seq, num_q_heads, block_size, cache_stride_bytes, k_scale, v_scale, sm_scale, out)
     _need(workspace, torch.uint8, "workspace")
-    o = options(num_ctas, tile_tokens, wait_limit_ns, ev_begin, ev_end)
+    o = options(num_ctas, tile_tokens, wait_limit_ns, ev_begin, ev_end, gather_mode)
     check(_lib.load().dsa_mla_decode_ws(*a, int(verify_rows), _ptr(workspace), workspace.numel(),
                                         _lib.ctypes.byref(o), _stream(stream)), "dsa_mla_decode_ws")
     return out
@@ -184,16 +186,16 @@ def _workload_args(w):
 
 
 def decode_workload(w, out=None, workspace=None, num_ctas=0, verify=None, stream=None, ev_begin=None,
-                    ev_end=None, tile_tokens=0, wait_limit_ns=0) -> torch.Tensor:
+                    ev_end=None, tile_tokens=0, wait_limit_ns=0, gather_mode=0) -> torch.Tensor:
     """Run the decode on a Workload. verify=True uses the k-row entry point with the
     workload's per-sequence base lengths. Per-call options (num_ctas, tile_tokens,
-    wait_limit_ns, events) go through dsa_mla_decode_ws; without a workspace one is
+    wait_limit_ns, gather_mode, events) go through dsa_mla_decode_ws; without a workspace one is
     allocated for the call."""
     q, kc, vc, bt, mbps = _workload_args(w)
     out = torch.empty_like(q) if out is None else out
     verify = (w.base_lens is not None) if verify is None else verify
     lens = w.base_lens if verify else w.seq_lens
-    if workspace is None and (num_ctas or tile_tokens or wait_limit_ns or ev_begin is not None):
+    if workspace is None and (num_ctas or tile_tokens or wait_limit_ns or gather_mode or ev_begin is not None):
         workspace = alloc_workspace(w.num_seqs, w.rows_per_seq, w.num_q_heads, w.sel_width, num_ctas,
                                     device=q.device)
     if workspace is None:
@@ -203,4 +205,5 @@ def decode_workload(w, out=None, workspace=None, num_ctas=0, verify=None, stream
     return decode_ws(q, kc, vc, bt, mbps, lens, w.sel_indices, w.num_seqs, w.rows_per_seq, w.num_q_heads,
                      w.block_size, w.cache_stride_bytes, w.k_scale, w.v_scale, w.sm_scale, out, workspace,
                      verify_rows=1 if verify else 0, num_ctas=num_ctas, ev_begin=ev_begin, ev_end=ev_end,
-                     tile_tokens=tile_tokens, wait_limit_ns=wait_limit_ns, stream=stream)
+                     tile_tokens=tile_tokens, wait_limit_ns=wait_limit_ns, gather_mode=gather_mode,
+                     stream=stream)

@@ -2,6 +2,8 @@
 // partition, workspace management and the launch sequence
 //   prologue (index resolution + query split) -> decode -> combine (when needed),
 // all enqueued on the caller's stream.
+#include <cudaTypedefs.h>
+
 #include <algorithm>
 #include <cstring>
 #include <mutex>
@@ -17,6 +19,7 @@ struct DeviceState {
     bool checked = false;
     int32_t status = DSA_OK;  // result of the device check
     int sms = 0;
+    size_t mem_bytes = 0;     // device memory size: bounds the rows a cache tensor map spans
     void* ws = nullptr;       // library-owned workspace
     size_t ws_bytes = 0;
 };
@@ -84,6 +87,9 @@ int32_t current_device(DeviceState** out) {
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return DSA_ERR_CUDA;
         d.sms = sms;
+        size_t free_b = 0, total_b = 0;
+        if (cudaMemGetInfo(&free_b, &total_b) != cudaSuccess) return DSA_ERR_CUDA;
+        d.mem_bytes = total_b;
         if (major != 10 || minor != 3) {
             d.status = DSA_ERR_UNSUPPORTED;
         } else {
@@ -111,6 +117,7 @@ struct Plan {
 struct CallOptions {
     int32_t num_ctas = 0;
     int32_t tile_tokens = 0;
+    int32_t gather_mode = 0;
     uint64_t wait_limit_ns = 0;
     cudaEvent_t ev0 = nullptr, ev1 = nullptr;
 };
@@ -122,8 +129,11 @@ int32_t read_options(const dsa_decode_options* o, CallOptions* out) {
     if (o) {
         if (o->num_ctas < 0) return DSA_ERR_INVALID_ARGUMENT;
         if (o->tile_tokens != 0 && o->tile_tokens != 64 && o->tile_tokens != 128) return DSA_ERR_INVALID_ARGUMENT;
+        if (o->gather_mode != 0 && o->gather_mode != 1) return DSA_ERR_INVALID_ARGUMENT;
+        if (o->reserved != 0) return DSA_ERR_INVALID_ARGUMENT;
         c.num_ctas = o->num_ctas;
         c.tile_tokens = o->tile_tokens;
+        c.gather_mode = o->gather_mode;
         c.wait_limit_ns = o->wait_limit_ns;
         c.ev0 = static_cast<cudaEvent_t>(o->ev_begin);
         c.ev1 = static_cast<cudaEvent_t>(o->ev_end);
@@ -157,7 +167,38 @@ Plan make_plan(int64_t rows, int32_t heads, int32_t width, int32_t num_ctas, int
     return pl;
 }
 
-int32_t enqueue(const Args& a, const Plan& pl, uint8_t* ws, const CallOptions& opt, cudaStream_t stream) {
+// cuTensorMapEncodeTiled from the driver, looked up once.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }();
+    return fn;
+}
+
+// 2-D map of a dense cache: rows of 512 bytes (row = page*block_size + slot), enough rows
+// to span the device's memory from the cache's base, read as boxes of 128 bytes x 1 row
+// into the 128-byte-swizzled operand layout; rows past the map are zero-filled.
+bool encode_cache_map(const void* base, size_t mem_bytes, CUtensorMap* m) {
+    const auto fn = tensor_map_encoder();
+    if (!fn) return false;
+    const cuuint64_t rows = std::min<cuuint64_t>(mem_bytes / kLatent + 1, (1ull << 31) - 1);
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kLatent), rows};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kLatent)};
+    const cuuint32_t box[2] = {128, 1};
+    const cuuint32_t estride[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estride,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int32_t enqueue(const Args& a, const Plan& pl, uint8_t* ws, const CallOptions& opt, size_t mem_bytes,
+                cudaStream_t stream) {
     const cudaEvent_t ev0 = opt.ev0, ev1 = opt.ev1;
     PrologueParams pp{};
     pp.sel = a.sel;
@@ -204,6 +245,16 @@ int32_t enqueue(const Args& a, const Plan& pl, uint8_t* ws, const CallOptions& o
     dp.v_scale = a.v_scale;
     dp.early_dependents = early ? 1 : 0;
     dp.wait_limit_ns = opt.wait_limit_ns;
+    // Tensor-map gathers need rows of one uniform stride (dense pages) and 128-byte
+    // aligned caches; anything else takes the per-thread copies.
+    CUtensorMap kmap, vmap;
+    std::memset(&kmap, 0, sizeof kmap);
+    std::memset(&vmap, 0, sizeof vmap);
+    dp.use_tma = 0;
+    if (opt.gather_mode == 0 && a.stride == static_cast<int64_t>(a.block_size) * kLatent && aligned(a.k_cache, 128) &&
+        aligned(a.v_cache, 128) && encode_cache_map(a.k_cache, mem_bytes, &kmap) &&
+        (dp.kv_same || encode_cache_map(a.v_cache, mem_bytes, &vmap)))
+        dp.use_tma = 1;
 #ifdef DSA_TRACE
     dp.trace = g_trace;
 #endif
@@ -216,7 +267,7 @@ int32_t enqueue(const Args& a, const Plan& pl, uint8_t* ws, const CallOptions& o
         if (cs == cudaStreamCaptureStatusActive) ev_flags = cudaEventRecordExternal;
     }
     if (ev0 && cudaEventRecordWithFlags(ev0, stream, ev_flags) != cudaSuccess) return DSA_ERR_CUDA;
-    st = from_cuda(pl.small_tiles ? launch_decode_64(dp, stream) : launch_decode_128(dp, stream));
+    st = from_cuda(pl.small_tiles ? launch_decode_64(dp, kmap, vmap, stream) : launch_decode_128(dp, kmap, vmap, stream));
     if (st != DSA_OK) return st;
     if (ev1 && cudaEventRecordWithFlags(ev1, stream, ev_flags) != cudaSuccess) return DSA_ERR_CUDA;
 
@@ -248,7 +299,7 @@ int32_t run_ws(const Args& a, void* workspace, size_t workspace_bytes, const dsa
     const Plan pl = make_plan(static_cast<int64_t>(a.num_seqs) * a.rows_per_seq, a.heads, a.width, opt.num_ctas,
                               d->sms, opt.tile_tokens);
     if (workspace_bytes < pl.ws.total) return DSA_ERR_WORKSPACE;
-    return enqueue(a, pl, static_cast<uint8_t*>(workspace), opt, stream);
+    return enqueue(a, pl, static_cast<uint8_t*>(workspace), opt, d->mem_bytes, stream);
 }
 
 int32_t run_lib(const Args& a, cudaStream_t stream) {
@@ -280,7 +331,7 @@ int32_t run_lib(const Args& a, cudaStream_t stream) {
     }
     CallOptions opt;
     read_options(nullptr, &opt);
-    return enqueue(a, pl, static_cast<uint8_t*>(ws), opt, stream);
+    return enqueue(a, pl, static_cast<uint8_t*>(ws), opt, d->mem_bytes, stream);
 }
 
 Args make_args(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
@@ -451,7 +502,7 @@ int32_t dsa_mla_decode_host(const void* q_host, const void* k_cache, const void*
                        verify_rows);
     CallOptions opt;
     read_options(nullptr, &opt);
-    st = enqueue(a, pl, ws, opt, s);
+    st = enqueue(a, pl, ws, opt, d->mem_bytes, s);
     if (st != DSA_OK) return st;
     if (cudaMemcpyAsync(out_host, ws + hs.out, qb, cudaMemcpyDeviceToHost, s) != cudaSuccess) return DSA_ERR_CUDA;
     return DSA_OK;

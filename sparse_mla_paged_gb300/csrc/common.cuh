@@ -5,6 +5,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "dsa_mla.h"
@@ -177,6 +178,7 @@ struct DecodeParams {
     float v_scale;
     int32_t early_dependents;  // let the next kernel launch once every CTA has started
     uint64_t wait_limit_ns;    // time limit of each pipeline wait (DSA_ERR_TIMEOUT past it)
+    int32_t use_tma;           // gather by tensor map (dense pages), else per-thread copies
     unsigned long long* trace;  // per-CTA timeline, used only by -DDSA_TRACE builds
 };
 
@@ -200,8 +202,12 @@ cudaError_t launch_prologue(const PrologueParams& p, int blocks, bool programmat
 // The decode kernel exists for tiles of 64 and of 128 tokens (decode.cu compiled twice);
 // 64-token tiles pipeline better when a CTA has little work, 128-token tiles use the
 // tensor core better when it has much.
-cudaError_t launch_decode_64(const DecodeParams& p, cudaStream_t stream);
-cudaError_t launch_decode_128(const DecodeParams& p, cudaStream_t stream);
+// kmap / vmap: 2-D tensor maps of the K and V caches ([rows of 512 bytes], box 128 x 1,
+// 128-byte swizzle), read only when p.use_tma is set.
+cudaError_t launch_decode_64(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                             cudaStream_t stream);
+cudaError_t launch_decode_128(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                              cudaStream_t stream);
 // max_pieces: the most CTAs sharing one unit (max_pieces_per_unit; selects the variant).
 cudaError_t launch_combine(const CombineParams& p, int units, int max_pieces, cudaStream_t stream);
 cudaError_t decode_kernel_setup_64();

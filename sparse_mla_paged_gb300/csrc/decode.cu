@@ -31,6 +31,7 @@
 // Shared memory 226 KB, TMEM 512 columns: O^T at 0..255 (chunk c of 128 dims at 64c),
 // query operand at 256..383, S at 384..511. Every wait is bounded (see ptx.cuh); on a
 // timeout the CTA records DSA_ERR_TIMEOUT, skips the remaining waits and finishes.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -270,6 +271,94 @@ __device__ void run_producer(const DecodeParams& p, uint32_t sbase, volatile int
 }
 
 // ------------------------------------------------------------------------------------
+// gather by tensor map (pages of block_size*512 bytes: token row = page*block_size + slot)
+// ------------------------------------------------------------------------------------
+// Warp 0 alone: lane l (l < kGroups4) fetches tokens 4l..4l+3 of every tile with one
+// tile::gather4 per 128-dim block, straight into the 128-byte-swizzled operand layout
+// (the swizzle follows the shared-memory address, and each token group's rows sit at
+// (tk/8)*4096 + kb*1024 + (tk%8)*128 of the slot). Rows without a token take index -1
+// and are zero-filled. One arrive.expect_tx per tile arms the slot's full barrier.
+constexpr int kGroups4 = kTileTokens / 4;
+
+__device__ void run_producer_tma(const DecodeParams& p, const CUtensorMap* kmap, const CUtensorMap* vmap,
+                                 uint32_t sbase, volatile int* abort_flag, int nseg, const Segment& seg0) {
+    const int lane = threadIdx.x & 31;
+    const Ring ring(p.kv_same);
+    const int64_t W = p.part.width;
+    const uint32_t tile_bytes = (p.kv_same ? 1u : 2u) * static_cast<uint32_t>(kKvTileBytes);
+    const bool active = lane < kGroups4;
+    const uint32_t lane_dst = ((4 * lane) >> 3) * kGroupBytes + ((4 * lane) & 7) * 128;
+    uint32_t tau = 0;
+    bool stop = false;
+    for (int i = 0; i < nseg && !stop; ++i) {
+        const Segment s = i == 0 ? seg0 : cta_segment(p.part, blockIdx.x, i);
+        const long long* offs = p.offs + static_cast<int64_t>(s.row) * W + s.s0;
+        const int32_t span = static_cast<int32_t>(s.s1 - s.s0);
+        // The first tile's offsets are requested together with the row's count.
+        long long o4[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) o4[k] = (active && 4 * lane + k < span) ? offs[4 * lane + k] : -1;
+        const Tiles tl = segment_tokens(p, s);
+        if (tl.n <= 0) continue;
+        for (int t = 0; t < tl.ntiles; ++t, ++tau) {
+            int32_t y[4];
+            bool bad = false;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const bool in = active && t * kTileTokens + 4 * lane + k < tl.n;
+                y[k] = (in && o4[k] >= 0) ? static_cast<int32_t>(o4[k] >> 9) : -1;
+                bad |= in && o4[k] < 0;
+            }
+            if (bad) atomicCAS(p.status, 0, kStatusBounds);
+            // next tile's offsets, before the slot wait
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int j = (t + 1) * kTileTokens + 4 * lane + k;
+                o4[k] = (active && t + 1 < tl.ntiles && j < tl.n) ? offs[j] : -1;
+            }
+            const int e = static_cast<int>(tau % ring.slots);
+            const uint32_t use = tau / ring.slots;
+            if (tau >= static_cast<uint32_t>(ring.slots))
+                warp_wait(p, sbase + kOffBars + 8 * (BAR_EMPTY0 + e), (use - 1) & 1, abort_flag);
+            // After a failed wait nothing more is issued: every copy in flight then targets a
+            // slot whose previous contents were consumed, and the drain below finds it.
+            if (__shfl_sync(0xffffffffu, *abort_flag, 0)) {
+                stop = true;
+                break;
+            }
+            if (tau < 8 && lane == 0) DSA_TRACE_AT(p, 40 + tau);
+            const uint32_t full = sbase + kOffBars + 8 * (BAR_FULL0 + e);
+            if (lane == 0) mbar_arrive_expect_tx(full, tile_bytes);
+            __syncwarp();
+            const uint32_t kdst = sbase + kOffRing + e * ring.slot_bytes + lane_dst;
+            if (active) {
+#pragma unroll
+                for (int kb = 0; kb < 4; ++kb)
+                    tma_gather4(kdst + kb * 1024, kmap, kb * 128, y[0], y[1], y[2], y[3], full);
+                if (!p.kv_same) {
+#pragma unroll
+                    for (int kb = 0; kb < 4; ++kb)
+                        tma_gather4(kdst + kKvTileBytes + kb * 1024, vmap, kb * 128, y[0], y[1], y[2], y[3], full);
+                }
+            }
+            if (tau < 8 && lane == 0) DSA_TRACE_AT(p, 48 + tau);
+        }
+    }
+    // Drain: only the last ring.slots tiles can still be landing; wait for each one's
+    // bytes (bounded) so that no copy into shared memory is in flight when the CTA exits.
+    if (lane == 0) {
+        const uint32_t first = tau > static_cast<uint32_t>(ring.slots) ? tau - ring.slots : 0;
+        for (uint32_t k = first; k < tau; ++k) {
+            const uint32_t bar = sbase + kOffBars + 8 * (BAR_FULL0 + static_cast<int>(k % ring.slots));
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(bar, (k / ring.slots) & 1) && globaltimer_ns() - t0 < kDrainLimitNs) {
+            }
+        }
+    }
+    __syncwarp();
+}
+
+// ------------------------------------------------------------------------------------
 // MMA warp (one thread issues)
 // ------------------------------------------------------------------------------------
 // Warp-uniform wait: every lane polls, the warp leaves together (lane 0 decides timeouts).
@@ -279,6 +368,10 @@ __device__ __forceinline__ bool warp_poll(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ void mma_wait(const DecodeParams& p, uint32_t bar, uint32_t parity,
                                          volatile int* abort_flag) {
     if (warp_poll(bar, parity)) return;
+    if (p.wait_limit_ns < kPollHintNs) {  // below the polling interval: give up at once
+        fail(p, abort_flag, kStatusTimeout);
+        return;
+    }
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
         mbar_try_wait_hint(bar, parity, kPollHintNs);
@@ -382,8 +475,10 @@ __device__ void run_mma(const DecodeParams& p, uint32_t sbase, uint32_t tmem, vo
                     pv_done = true;
                 }
                 if (!qk_done || !pv_done) {
-                    const bool give_up =
-                        __shfl_sync(0xffffffffu, (*abort_flag != 0) || globaltimer_ns() - t_start > p.wait_limit_ns, 0);
+                    const bool give_up = __shfl_sync(0xffffffffu,
+                                                     (*abort_flag != 0) || p.wait_limit_ns < kPollHintNs ||
+                                                         globaltimer_ns() - t_start > p.wait_limit_ns,
+                                                     0);
                     if (give_up) {
                         fail(p, abort_flag, kStatusTimeout);
                         break;
@@ -699,7 +794,9 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
     if (st == 0) DSA_TRACE_AT(p, 19);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
+                  const __grid_constant__ CUtensorMap vmap) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -710,8 +807,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     if (tid == 0) {
         const uint32_t b = sbase + kOffBars;
         for (int e = 0; e < kSlotsKV; ++e) {
-            // one copy-completion arrival per gather lane
-            mbar_init(b + 8 * (BAR_FULL0 + e), 32 * kProducerWarps);
+            // tensor-map gather: one arrive.expect_tx per tile; per-thread copies: one
+            // copy-completion arrival per gather lane
+            mbar_init(b + 8 * (BAR_FULL0 + e), p.use_tma ? 1 : 32 * kProducerWarps);
             mbar_init(b + 8 * (BAR_EMPTY0 + e), 1);
         }
         for (int k = 0; k < kSBufs; ++k) {
@@ -729,6 +827,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
         mbar_init(b + 8 * BAR_DONE, kSoftmaxWarps);
         *abort_flag = 0;
         fence_mbar_init();
+        if (p.use_tma) {
+            prefetch_tmap(&kmap);
+            if (!p.kv_same) prefetch_tmap(&vmap);
+        }
     }
     if (warp == kMmaWarp) {
         tmem_alloc(sbase + kOffTmemSlot, kTmemCols);
@@ -753,7 +855,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     if (p.early_dependents) griddep_launch_dependents();
 
     if (warp < kProducerWarps) {
-        run_producer(p, sbase, abort_flag, nseg, seg0);
+        if (!p.use_tma)
+            run_producer(p, sbase, abort_flag, nseg, seg0);
+        else if (warp == 0)
+            run_producer_tma(p, &kmap, &vmap, sbase, abort_flag, nseg, seg0);
     } else if (warp == kMmaWarp) {
         run_mma(p, sbase, tmem, abort_flag, nseg, seg0);
         // Wait (bounded, regardless of abort) until every issued MMA has completed and the
@@ -800,7 +905,8 @@ cudaError_t DSA_CAT(decode_kernel_setup_, DSA_TILE)() {
     return cudaFuncSetAttribute(decode_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
 }
 
-cudaError_t DSA_CAT(launch_decode_, DSA_TILE)(const DecodeParams& p, cudaStream_t stream) {
+cudaError_t DSA_CAT(launch_decode_, DSA_TILE)(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                              cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.part.ctas);
     cfg.blockDim = dim3(kThreads);
@@ -811,7 +917,7 @@ cudaError_t DSA_CAT(launch_decode_, DSA_TILE)(const DecodeParams& p, cudaStream_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_kernel, p);
+    return cudaLaunchKernelEx(&cfg, decode_kernel, p, kmap, vmap);
 }
 
 }  // namespace dsa

@@ -72,10 +72,13 @@ constexpr uint32_t kPollHintNs = 500;
 // Waits for the phase with the given parity to complete. Returns false if the wait
 // ran out of time (limit_ns) or the abort flag was raised meanwhile.
 // The suspend hint never exceeds the limit, so a short limit is not hidden by a long
-// suspension that the phase happens to end.
+// suspension that the phase happens to end. %globaltimer may advance in steps coarser
+// than the polling interval, so a limit below kPollHintNs gives up at once when the
+// phase is not complete at the first poll.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort_flag,
                                           uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (limit_ns < kPollHintNs) return false;
     const uint32_t hint = limit_ns < kSuspendHintNs ? static_cast<uint32_t>(limit_ns) : kSuspendHintNs;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
@@ -110,6 +113,23 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
         "l"(src), "r"(bytes), "r"(bar)
         : "memory");
+}
+// Tensor-map gather of four rows (tile::gather4): from the 2-D map `tmap` (a kernel
+// parameter's generic address), the box of the map's width at column x of rows y0..y3 is
+// written to shared memory at dst as four consecutive box rows, laid out by the map's
+// swizzle mode; rows outside the map (a negative index included) are filled with zeros.
+// Completion is counted in bytes on the mbarrier. The map's box must be one row high.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int32_t x, int32_t y0, int32_t y1,
+                                            int32_t y2, int32_t y3, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(tmap), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
+        : "memory");
+}
+// Brings a tensor map (kernel parameter) into the descriptor cache ahead of its first use.
+__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 // Orders this thread's generic-proxy shared-memory accesses with later async-proxy
 // accesses (tensor-core operand reads).

@@ -82,7 +82,8 @@ def test_decode_ws_rejects_bad_workspace_on_host(lib):
 
 
 @pytest.mark.parametrize("field,value", [("num_ctas", -1), ("tile_tokens", -1), ("tile_tokens", 1),
-                                         ("tile_tokens", 32), ("tile_tokens", 96), ("tile_tokens", 256)])
+                                         ("tile_tokens", 32), ("tile_tokens", 96), ("tile_tokens", 256),
+                                         ("gather_mode", -1), ("gather_mode", 2), ("reserved", 1)])
 def test_decode_ws_rejects_bad_options_on_host(lib, field, value):
     o = _lib.DecodeOptions()
     setattr(o, field, value)
@@ -95,8 +96,8 @@ def test_options_struct_matches_the_header():
     body = re.search(r"typedef struct dsa_decode_options \{(.*?)\} dsa_decode_options;", text, re.S).group(1)
     fields = re.findall(r"(\w+)\s*;", body)
     assert fields == [f for f, _ in _lib.DecodeOptions._fields_]
-    assert ctypes.sizeof(_lib.DecodeOptions) == 32
-    assert _lib.DecodeOptions.wait_limit_ns.offset == 8 and _lib.DecodeOptions.ev_begin.offset == 16
+    assert ctypes.sizeof(_lib.DecodeOptions) == 40
+    assert _lib.DecodeOptions.wait_limit_ns.offset == 16 and _lib.DecodeOptions.ev_begin.offset == 24
 
 
 def test_resolve_rejects_bad_arguments_on_host(lib):

@@ -354,3 +354,19 @@ def test_wait_timeout_sets_device_status_and_recovers(api):
     torch.cuda.synchronize()
     assert api.read_device_status(ws) == 0
     assert_parity(out, oracle.decode_workload(w), "after a timed-out call")
+
+
+# ------------------------------------------------------------------------------------
+# The two gather paths (tensor-map gathers, per-thread copies) fill the same operand
+# layout, so the decode gives bit-identical outputs through either.
+# ------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("tile", [64, 128])
+@pytest.mark.parametrize("name", ["ragged 3 tiles", "many tiles", "130 heads", "block size 1", "block size 100",
+                                  "split K/V many tiles", "multi seq", "rows per seq", "heavy tails"])
+def test_gather_paths_agree(api, name, tile):
+    w = wl.random_case(seed=zlib.crc32(name.encode()) % 100000, **CASES[name]).to("cuda")
+    a = api.decode_workload(w, tile_tokens=tile, gather_mode=0)
+    b = api.decode_workload(w, tile_tokens=tile, gather_mode=1)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
