@@ -367,11 +367,11 @@ __device__ __forceinline__ bool warp_poll(uint32_t bar, uint32_t parity) {
 }
 __device__ __forceinline__ void mma_wait(const DecodeParams& p, uint32_t bar, uint32_t parity,
                                          volatile int* abort_flag) {
-    if (warp_poll(bar, parity)) return;
-    if (p.wait_limit_ns < kPollHintNs) {  // below the polling interval: give up at once
-        fail(p, abort_flag, kStatusTimeout);
+    if (p.wait_limit_ns < kPollHintNs) {  // below the polling interval: one non-blocking test
+        if (!__all_sync(0xffffffffu, mbar_test_wait(bar, parity) != 0)) fail(p, abort_flag, kStatusTimeout);
         return;
     }
+    if (warp_poll(bar, parity)) return;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
         mbar_try_wait_hint(bar, parity, kPollHintNs);

@@ -53,6 +53,19 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity)
         : "memory");
     return ok;
 }
+// Non-blocking test of the phase with the given parity (try_wait may suspend the thread
+// for a system-dependent time while the phase is incomplete; test_wait never does).
+__device__ __forceinline__ uint32_t mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok;
+}
 // Longest time a waiting thread stays suspended (not issuing) in one try_wait while the
 // phase is incomplete; it resumes as soon as the phase completes.
 constexpr uint32_t kSuspendHintNs = 20000;
@@ -72,13 +85,13 @@ constexpr uint32_t kPollHintNs = 500;
 // Waits for the phase with the given parity to complete. Returns false if the wait
 // ran out of time (limit_ns) or the abort flag was raised meanwhile.
 // The suspend hint never exceeds the limit, so a short limit is not hidden by a long
-// suspension that the phase happens to end. %globaltimer may advance in steps coarser
-// than the polling interval, so a limit below kPollHintNs gives up at once when the
-// phase is not complete at the first poll.
+// suspension that the phase happens to end. A limit below kPollHintNs (finer than the
+// polling interval, and than %globaltimer's steps may be) makes the wait a single
+// non-blocking test: it gives up at once when the phase is not complete.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort_flag,
                                           uint64_t limit_ns) {
+    if (limit_ns < kPollHintNs) return mbar_test_wait(bar, parity) != 0;
     if (mbar_try_wait(bar, parity)) return true;
-    if (limit_ns < kPollHintNs) return false;
     const uint32_t hint = limit_ns < kSuspendHintNs ? static_cast<uint32_t>(limit_ns) : kSuspendHintNs;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
