@@ -513,8 +513,8 @@ def main():
     ap.add_argument("--ctas", type=int, default=0, help="decode grid size (0 = library default)")
     ap.add_argument("--tile", type=int, default=0, choices=[0, 64, 128],
                     help="decode tile in tokens (0 = library default)")
-    ap.add_argument("--gather-mode", type=int, default=0, choices=[0, 1],
-                    help="0 = library default (tensor-map gathers on dense pages), 1 = per-thread copies")
+    ap.add_argument("--gather-mode", type=int, default=0, choices=[0, 1, 2],
+                    help="0 = library default, 1 = per-thread copies, 2 = tensor-map gathers on dense pages")
     ap.add_argument("--replicas", type=int, default=0)
     ap.add_argument("--seqs", type=int, default=0,
                     help="sequences per batch (0 = the workload's own count); smaller batches serve "

@@ -141,11 +141,12 @@ size_t dsa_mla_decode_workspace_bytes(int32_t num_seqs, int32_t rows_per_seq,
  *  tile_tokens    KV tokens per decode tile: 0 = automatic (64-token tiles when each
  *                 decode CTA has at most 256 selected slots of work, 128 otherwise),
  *                 64 or 128 = that size. Any other value is DSA_ERR_INVALID_ARGUMENT.
- *  gather_mode    how the decode fetches cache rows: 0 = automatic (tensor-map gathers
- *                 when the pages are dense, cache_stride_bytes = block_size*512, and the
- *                 caches are 128-byte aligned; per-thread 16-byte copies otherwise),
- *                 1 = per-thread copies always. Any other value is
- *                 DSA_ERR_INVALID_ARGUMENT.
+ *  gather_mode    how the decode fetches cache rows: 0 = default (per-thread 16-byte
+ *                 copies), 1 = per-thread copies, 2 = tensor-map four-row gathers when
+ *                 the pages are dense (cache_stride_bytes = block_size*512) and the caches
+ *                 are 128-byte aligned, per-thread copies otherwise. The gathers give the
+ *                 same results; on GB300 they measured slower than the copies. Any other
+ *                 value is DSA_ERR_INVALID_ARGUMENT.
  *  wait_limit_ns  time limit of every pipeline wait inside the decode kernel; 0 = the
  *                 default of one second. A wait that runs out records DSA_ERR_TIMEOUT in
  *                 the status word, stops the kernel's pipeline and leaves the output

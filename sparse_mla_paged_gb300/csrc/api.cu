@@ -129,7 +129,7 @@ int32_t read_options(const dsa_decode_options* o, CallOptions* out) {
     if (o) {
         if (o->num_ctas < 0) return DSA_ERR_INVALID_ARGUMENT;
         if (o->tile_tokens != 0 && o->tile_tokens != 64 && o->tile_tokens != 128) return DSA_ERR_INVALID_ARGUMENT;
-        if (o->gather_mode != 0 && o->gather_mode != 1) return DSA_ERR_INVALID_ARGUMENT;
+        if (o->gather_mode < 0 || o->gather_mode > 2) return DSA_ERR_INVALID_ARGUMENT;
         if (o->reserved != 0) return DSA_ERR_INVALID_ARGUMENT;
         c.num_ctas = o->num_ctas;
         c.tile_tokens = o->tile_tokens;
@@ -193,7 +193,7 @@ bool encode_cache_map(const void* base, size_t mem_bytes, CUtensorMap* m) {
     const cuuint32_t box[2] = {128, 1};
     const cuuint32_t estride[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estride,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -245,13 +245,13 @@ int32_t enqueue(const Args& a, const Plan& pl, uint8_t* ws, const CallOptions& o
     dp.v_scale = a.v_scale;
     dp.early_dependents = early ? 1 : 0;
     dp.wait_limit_ns = opt.wait_limit_ns;
-    // Tensor-map gathers need rows of one uniform stride (dense pages) and 128-byte
-    // aligned caches; anything else takes the per-thread copies.
+    // Tensor-map gathers (on request) need rows of one uniform stride (dense pages) and
+    // 128-byte aligned caches; anything else takes the per-thread copies.
     CUtensorMap kmap, vmap;
     std::memset(&kmap, 0, sizeof kmap);
     std::memset(&vmap, 0, sizeof vmap);
     dp.use_tma = 0;
-    if (opt.gather_mode == 0 && a.stride == static_cast<int64_t>(a.block_size) * kLatent && aligned(a.k_cache, 128) &&
+    if (opt.gather_mode == 2 && a.stride == static_cast<int64_t>(a.block_size) * kLatent && aligned(a.k_cache, 128) &&
         aligned(a.v_cache, 128) && encode_cache_map(a.k_cache, mem_bytes, &kmap) &&
         (dp.kv_same || encode_cache_map(a.v_cache, mem_bytes, &vmap)))
         dp.use_tma = 1;

@@ -365,13 +365,13 @@ __device__ void run_producer_tma(const DecodeParams& p, const CUtensorMap* kmap,
 __device__ __forceinline__ bool warp_poll(uint32_t bar, uint32_t parity) {
     return __all_sync(0xffffffffu, mbar_try_wait(bar, parity) != 0);
 }
-__device__ __forceinline__ void mma_wait(const DecodeParams& p, uint32_t bar, uint32_t parity,
-                                         volatile int* abort_flag) {
-    if (p.wait_limit_ns < kPollHintNs) {  // below the polling interval: one non-blocking test
-        if (!__all_sync(0xffffffffu, mbar_test_wait(bar, parity) != 0)) fail(p, abort_flag, kStatusTimeout);
+// Slow path of mma_wait, out of line (see mbar_wait).
+static __device__ __noinline__ void mma_wait_slow(const DecodeParams& p, uint32_t bar, uint32_t parity,
+                                           volatile int* abort_flag) {
+    if (p.wait_limit_ns < kPollHintNs) {  // below the polling interval: the test has failed
+        fail(p, abort_flag, kStatusTimeout);
         return;
     }
-    if (warp_poll(bar, parity)) return;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
         mbar_try_wait_hint(bar, parity, kPollHintNs);
@@ -383,6 +383,13 @@ __device__ __forceinline__ void mma_wait(const DecodeParams& p, uint32_t bar, ui
             return;
         }
     }
+}
+__device__ __forceinline__ void mma_wait(const DecodeParams& p, uint32_t bar, uint32_t parity,
+                                         volatile int* abort_flag) {
+    // Below the polling interval a single non-blocking test decides.
+    const bool done = p.wait_limit_ns < kPollHintNs ? __all_sync(0xffffffffu, mbar_test_wait(bar, parity) != 0)
+                                                     : warp_poll(bar, parity);
+    if (!done) mma_wait_slow(p, bar, parity, abort_flag);
 }
 
 // The whole MMA warp runs this loop converged; the elected lane issues.
@@ -628,16 +635,17 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
             // its half, the lo lane the last kScores.
             const int tok0 = t * kTileTokens + half * kHalfCols + term * kScores;
             float x[kScores];
-            float hmax = kNegInf;
+            float hm4[4] = {kNegInf, kNegInf, kNegInf, kNegInf};  // four independent max chains
 #pragma unroll
             for (int j = 0; j < kScores; ++j) {
                 const float send = __uint_as_float(term ? v[j] : v[kScores + j]);
                 const float mine = __uint_as_float(term ? v[kScores + j] : v[j]);
                 const float other = __shfl_xor_sync(0xffffffffu, send, 1);
                 x[j] = (tok0 + j < tl.n) ? (mine + other) * c : kNegInf;
-                hmax = fmaxf(hmax, x[j]);
+                hm4[j & 3] = fmaxf(hm4[j & 3], x[j]);
             }
             // Max of head hq over this warp's half of the tile.
+            float hmax = fmaxf(fmaxf(hm4[0], hm4[1]), fmaxf(hm4[2], hm4[3]));
             hmax = fmaxf(hmax, __shfl_xor_sync(0xffffffffu, hmax, 1));
             const bool over = hmax > m_ref + kRescaleMargin;
             const bool under = hmax < m_ref - kRescaleDrop && m_ref > m_top - kRescaleFloor;
@@ -679,21 +687,22 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
 
             // P' = 2^(x - m + kPBias) as two E4M3 terms, 16 tokens per 16-byte row.
             uint32_t hw[kScores / 4], lw[kScores / 4];
-            float lsum = 0.0f;
+            float ls4[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // four independent sum chains
+            const float off = kPBias - m_ref;
 #pragma unroll
             for (int g = 0; g < kScores / 4; ++g) {
                 float ph[4], pl[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float pp = ex2_approx(x[4 * g + e] - m_ref + kPBias);
-                    lsum += pp;
+                    const float pp = ex2_approx(x[4 * g + e] + off);
+                    ls4[e] += pp;
                     ph[e] = hi_part(pp);
                     pl[e] = pp - ph[e];
                 }
                 hw[g] = pack_e4m3x4(ph[0], ph[1], ph[2], ph[3]);
                 lw[g] = pack_e4m3x4(pl[0], pl[1], pl[2], pl[3]);
             }
-            l_part += lsum;
+            l_part += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
             if (st == 0 && (tau == 2 || tau == 3)) DSA_TRACE_AT(p, 74 + 8 * (tau - 2));
             // P buffer tau%2 is free once the P.V two tiles back has finished reading it.
             if (tau >= 2) warp_wait(p, barp(BAR_PVDONE0 + (tau & 1)), ((tau >> 1) - 1) & 1, abort_flag);
@@ -794,9 +803,12 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
     if (st == 0) DSA_TRACE_AT(p, 19);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-    decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
-                  const __grid_constant__ CUtensorMap vmap) {
+// kTma: gather by tensor map (warp 0) or by per-thread copies (warps 0-2). The two are
+// separate kernels so that each carries only its own gather code (the warps of one CTA
+// run different code at once and share the SM's instruction cache) and the per-thread
+// copy kernel takes no tensor maps.
+template <bool kTma>
+__device__ __forceinline__ void decode_body(const DecodeParams& p, const CUtensorMap* kmap, const CUtensorMap* vmap) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -809,7 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < kSlotsKV; ++e) {
             // tensor-map gather: one arrive.expect_tx per tile; per-thread copies: one
             // copy-completion arrival per gather lane
-            mbar_init(b + 8 * (BAR_FULL0 + e), p.use_tma ? 1 : 32 * kProducerWarps);
+            mbar_init(b + 8 * (BAR_FULL0 + e), kTma ? 1 : 32 * kProducerWarps);
             mbar_init(b + 8 * (BAR_EMPTY0 + e), 1);
         }
         for (int k = 0; k < kSBufs; ++k) {
@@ -827,9 +839,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(b + 8 * BAR_DONE, kSoftmaxWarps);
         *abort_flag = 0;
         fence_mbar_init();
-        if (p.use_tma) {
-            prefetch_tmap(&kmap);
-            if (!p.kv_same) prefetch_tmap(&vmap);
+        if (kTma) {
+            prefetch_tmap(kmap);
+            if (!p.kv_same) prefetch_tmap(vmap);
         }
     }
     if (warp == kMmaWarp) {
@@ -855,10 +867,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.early_dependents) griddep_launch_dependents();
 
     if (warp < kProducerWarps) {
-        if (!p.use_tma)
+        if constexpr (!kTma)
             run_producer(p, sbase, abort_flag, nseg, seg0);
         else if (warp == 0)
-            run_producer_tma(p, &kmap, &vmap, sbase, abort_flag, nseg, seg0);
+            run_producer_tma(p, kmap, vmap, sbase, abort_flag, nseg, seg0);
     } else if (warp == kMmaWarp) {
         run_mma(p, sbase, tmem, abort_flag, nseg, seg0);
         // Wait (bounded, regardless of abort) until every issued MMA has completed and the
@@ -890,19 +902,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams p) {
+    decode_body<false>(p, nullptr, nullptr);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_kernel_tma(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
+                      const __grid_constant__ CUtensorMap vmap) {
+    decode_body<true>(p, &kmap, &vmap);
+}
+
 }  // namespace DSA_CAT(tile, DSA_TILE)
 
 using namespace DSA_CAT(tile, DSA_TILE);
 
-cudaError_t DSA_CAT(decode_kernel_setup_, DSA_TILE)() {
+template <typename K>
+cudaError_t setup_instance(K kernel) {
     // The register cap above must leave room for all kThreads threads of the block.
     cudaFuncAttributes attr;
-    cudaError_t e = cudaFuncGetAttributes(&attr, decode_kernel);
+    cudaError_t e = cudaFuncGetAttributes(&attr, kernel);
     if (e != cudaSuccess) return e;
     if (attr.maxThreadsPerBlock < kThreads) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(decode_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+}
+
+cudaError_t DSA_CAT(decode_kernel_setup_, DSA_TILE)() {
+    const cudaError_t e = setup_instance(decode_kernel);
+    return e != cudaSuccess ? e : setup_instance(decode_kernel_tma);
 }
 
 cudaError_t DSA_CAT(launch_decode_, DSA_TILE)(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
@@ -917,7 +945,8 @@ cudaError_t DSA_CAT(launch_decode_, DSA_TILE)(const DecodeParams& p, const CUten
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_kernel, p, kmap, vmap);
+    return p.use_tma ? cudaLaunchKernelEx(&cfg, decode_kernel_tma, p, kmap, vmap)
+                     : cudaLaunchKernelEx(&cfg, decode_kernel, p);
 }
 
 }  // namespace dsa

@@ -87,11 +87,12 @@ constexpr uint32_t kPollHintNs = 500;
 // The suspend hint never exceeds the limit, so a short limit is not hidden by a long
 // suspension that the phase happens to end. A limit below kPollHintNs (finer than the
 // polling interval, and than %globaltimer's steps may be) makes the wait a single
-// non-blocking test: it gives up at once when the phase is not complete.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort_flag,
-                                          uint64_t limit_ns) {
-    if (limit_ns < kPollHintNs) return mbar_test_wait(bar, parity) != 0;
-    if (mbar_try_wait(bar, parity)) return true;
+// non-blocking test: it gives up at once when the phase is not complete. The polling loop
+// is kept out of line: waits sit at many places in the kernel and its warps share one
+// instruction cache.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const volatile int* abort_flag,
+                                            uint64_t limit_ns) {
+    if (limit_ns < kPollHintNs) return false;
     const uint32_t hint = limit_ns < kSuspendHintNs ? static_cast<uint32_t>(limit_ns) : kSuspendHintNs;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
@@ -99,6 +100,11 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort_flag,
+                                          uint64_t limit_ns) {
+    if (limit_ns < kPollHintNs ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, abort_flag, limit_ns);
 }
 
 // ------------------------------------------------------------------------------------

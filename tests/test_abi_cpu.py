@@ -83,7 +83,7 @@ def test_decode_ws_rejects_bad_workspace_on_host(lib):
 
 @pytest.mark.parametrize("field,value", [("num_ctas", -1), ("tile_tokens", -1), ("tile_tokens", 1),
                                          ("tile_tokens", 32), ("tile_tokens", 96), ("tile_tokens", 256),
-                                         ("gather_mode", -1), ("gather_mode", 2), ("reserved", 1)])
+                                         ("gather_mode", -1), ("gather_mode", 3), ("reserved", 1)])
 def test_decode_ws_rejects_bad_options_on_host(lib, field, value):
     o = _lib.DecodeOptions()
     setattr(o, field, value)
