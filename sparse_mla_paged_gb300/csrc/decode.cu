@@ -182,6 +182,16 @@ struct Ring {
 // ------------------------------------------------------------------------------------
 // gather warps
 // ------------------------------------------------------------------------------------
+// Asks L2 for the four 128-byte lines of the 512-byte row at byte offset o (nothing for
+// o < 0); no data comes back to the thread.
+__device__ __forceinline__ void prefetch_row_l2(const uint8_t* base, long long o) {
+    if (o >= 0) {
+        const uint8_t* r = base + o;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) asm volatile("prefetch.global.L2 [%0];" ::"l"(r + 128 * k));
+    }
+}
+
 // Rows of a tile taken by gather warp w: [w*43, min(w*43 + 43, 128)).
 constexpr int kWarpRows = (kTileTokens + kProducerWarps - 1) / kProducerWarps;
 
@@ -215,10 +225,27 @@ __device__ void run_producer(const DecodeParams& p, uint32_t sbase, volatile int
         };
         long long oa = (r0 + lane < tl.n) ? pa : -1;
         long long ob = (lane + 32 < nr && r0 + 32 + lane < tl.n) ? pb : -1;
+        // Offsets of the next tile (na, nb) and of the one after (fa, fb). At iteration t the
+        // latter belong to tile t + 2 and were requested an iteration earlier, so the L2
+        // prefetch of their rows does not wait on them; the copies of each tile then find
+        // their rows in L2 instead of waiting on DRAM.
+        long long na, nb, fa, fb;
+        load(1, na, nb);
+        load(2, fa, fb);
         for (int t = 0; t < tl.ntiles; ++t, ++tau) {
             const long long ca = oa, cb = ob;
             if (tid == 0 && t == 0 && i == 0 && ca != 12345) DSA_TRACE_AT(p, 5);
-            load(t + 1, oa, ob);  // next tile's rows, before the slot wait
+            prefetch_row_l2(p.k_cache, fa);
+            prefetch_row_l2(p.k_cache, fb);
+            if (!p.kv_same) {
+                prefetch_row_l2(p.v_cache, fa);
+                prefetch_row_l2(p.v_cache, fb);
+            }
+            oa = na;
+            ob = nb;
+            na = fa;
+            nb = fb;
+            load(t + 3, fa, fb);  // before the slot wait
             if (tid == 0 && t == 0 && i == 0) DSA_TRACE_AT(p, 6);
             if ((ca < 0 && t * kTileTokens + r0 + lane < tl.n) ||
                 (cb < 0 && lane + 32 < nr && t * kTileTokens + r0 + 32 + lane < tl.n))
@@ -641,9 +668,15 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
                 const float send = __uint_as_float(term ? v[j] : v[kScores + j]);
                 const float mine = __uint_as_float(term ? v[kScores + j] : v[j]);
                 const float other = __shfl_xor_sync(0xffffffffu, send, 1);
-                x[j] = (tok0 + j < tl.n) ? (mine + other) * c : kNegInf;
-                hm4[j & 3] = fmaxf(hm4[j & 3], x[j]);
+                x[j] = (mine + other) * c;
             }
+            if (t == tl.ntiles - 1) {  // only the last tile can hold positions past the count
+#pragma unroll
+                for (int j = 0; j < kScores; ++j)
+                    if (tok0 + j >= tl.n) x[j] = kNegInf;
+            }
+#pragma unroll
+            for (int j = 0; j < kScores; ++j) hm4[j & 3] = fmaxf(hm4[j & 3], x[j]);
             // Max of head hq over this warp's half of the tile.
             float hmax = fmaxf(fmaxf(hm4[0], hm4[1]), fmaxf(hm4[2], hm4[3]));
             hmax = fmaxf(hmax, __shfl_xor_sync(0xffffffffu, hmax, 1));
