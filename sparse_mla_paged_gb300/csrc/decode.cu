@@ -182,26 +182,28 @@ struct Ring {
 // ------------------------------------------------------------------------------------
 // gather warps
 // ------------------------------------------------------------------------------------
-// Asks L2 for the four 128-byte lines of the 512-byte row at byte offset o (nothing for
-// o < 0); no data comes back to the thread.
-__device__ __forceinline__ void prefetch_row_l2(const uint8_t* base, long long o) {
-    if (o >= 0) {
-        const uint8_t* r = base + o;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) asm volatile("prefetch.global.L2 [%0];" ::"l"(r + 128 * k));
-    }
-}
-
-// Rows of a tile taken by gather warp w: [w*43, min(w*43 + 43, 128)).
-constexpr int kWarpRows = (kTileTokens + kProducerWarps - 1) / kProducerWarps;
+// The tile's rows are dealt out in groups of 8 (one swizzle group each): warp w takes
+// groups [g0, g0 + ng), 6/5/5 groups for 128-token tiles and 3/3/2 for 64-token tiles.
+// Every warp's rows then start at a multiple of 8, so within a group the swizzle term of a
+// row depends only on the lane and the row's compile-time index: a row costs one shuffle
+// of its offset, one address add and one cp.async.
+constexpr int kGroups8 = kTileTokens / 8;
+constexpr int kWarpGroupsMax = (kGroups8 + kProducerWarps - 1) / kProducerWarps;
+static_assert(kWarpGroupsMax * 8 <= 64, "a warp's rows fit two offsets per lane");
 
 __device__ void run_producer(const DecodeParams& p, uint32_t sbase, volatile int* abort_flag, int nseg,
                              const Segment& seg0) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const Ring ring(p.kv_same);
     const int64_t W = p.part.width;
-    const int r0 = warp * kWarpRows;
-    const int nr = min(kWarpRows, kTileTokens - r0);
+    const int ng = kGroups8 / kProducerWarps + (warp < kGroups8 % kProducerWarps ? 1 : 0);
+    const int g0 = warp * (kGroups8 / kProducerWarps) + min(warp, kGroups8 % kProducerWarps);
+    const int r0 = 8 * g0;
+    const int nr = 8 * ng;
+    const uint32_t lane_dst = static_cast<uint32_t>(g0) * kGroupBytes + (lane >> 3) * 1024;
+    const uint32_t lx = lane & 7;
+    const uint8_t* kbase = p.k_cache + lane * 16;
+    const uint8_t* vbase = p.v_cache + lane * 16;
     uint32_t tau = 0;
     if (tid == 0) DSA_TRACE_AT(p, 2);
     for (int i = 0; i < nseg; ++i) {
@@ -225,27 +227,10 @@ __device__ void run_producer(const DecodeParams& p, uint32_t sbase, volatile int
         };
         long long oa = (r0 + lane < tl.n) ? pa : -1;
         long long ob = (lane + 32 < nr && r0 + 32 + lane < tl.n) ? pb : -1;
-        // Offsets of the next tile (na, nb) and of the one after (fa, fb). At iteration t the
-        // latter belong to tile t + 2 and were requested an iteration earlier, so the L2
-        // prefetch of their rows does not wait on them; the copies of each tile then find
-        // their rows in L2 instead of waiting on DRAM.
-        long long na, nb, fa, fb;
-        load(1, na, nb);
-        load(2, fa, fb);
         for (int t = 0; t < tl.ntiles; ++t, ++tau) {
             const long long ca = oa, cb = ob;
             if (tid == 0 && t == 0 && i == 0 && ca != 12345) DSA_TRACE_AT(p, 5);
-            prefetch_row_l2(p.k_cache, fa);
-            prefetch_row_l2(p.k_cache, fb);
-            if (!p.kv_same) {
-                prefetch_row_l2(p.v_cache, fa);
-                prefetch_row_l2(p.v_cache, fb);
-            }
-            oa = na;
-            ob = nb;
-            na = fa;
-            nb = fb;
-            load(t + 3, fa, fb);  // before the slot wait
+            load(t + 1, oa, ob);  // next tile's offsets, before the slot wait
             if (tid == 0 && t == 0 && i == 0) DSA_TRACE_AT(p, 6);
             if ((ca < 0 && t * kTileTokens + r0 + lane < tl.n) ||
                 (cb < 0 && lane + 32 < nr && t * kTileTokens + r0 + 32 + lane < tl.n))
@@ -256,37 +241,24 @@ __device__ void run_producer(const DecodeParams& p, uint32_t sbase, volatile int
             if (tau >= static_cast<uint32_t>(ring.slots))
                 warp_wait(p, sbase + kOffBars + 8 * (BAR_EMPTY0 + e), (use - 1) & 1, abort_flag);
             if (tid == 0 && tau < 8) DSA_TRACE_AT(p, 40 + tau);
-            const uint32_t kdst = sbase + kOffRing + e * ring.slot_bytes;
+            const uint32_t kdst = sbase + kOffRing + e * ring.slot_bytes + lane_dst;
             const uint32_t vdst = kdst + kKvTileBytes;
-            // Branch-free copy loop (a branch on the shuffled offset would serialise the
-            // copies): rows without a token (o < 0) are zero-filled by a source size of 0.
-            // Each row's offset is broadcast from the lane holding it. Offsets below 64 GiB
-            // travel as 32-bit counts of 16-byte units (one shuffle per row; 0xFFFFFFFF marks
-            // a row without token); a tile with a larger offset takes the 64-bit path.
-            const uint8_t* kbase = p.k_cache + lane * 16;
-            const uint8_t* vbase = p.v_cache + lane * 16;
-            auto copy_row = [&](long long o, int tk) {
-                const uint32_t d = (tk >> 3) * kGroupBytes + (lane >> 3) * 1024 + (tk & 7) * 128 +
-                                   (((lane & 7) ^ (tk & 7)) << 4);
-                const bool ok = o >= 0;
-                const uint64_t src = ok ? static_cast<uint64_t>(o) : 0;
-                cp_async_16_zfill(kdst + d, kbase + src, ok ? 16u : 0u);
-                if (!p.kv_same) cp_async_16_zfill(vdst + d, vbase + src, ok ? 16u : 0u);
-            };
-            constexpr long long kNarrow = 1ll << 36;
-            if (!__any_sync(0xffffffffu, ca >= kNarrow || cb >= kNarrow)) {
-                auto to16 = [](long long o) { return o >= 0 ? static_cast<uint32_t>(o >> 4) : 0xFFFFFFFFu; };
-                auto from16 = [](uint32_t u) { return u != 0xFFFFFFFFu ? static_cast<long long>(u) << 4 : -1ll; };
-                const uint32_t ua = to16(ca), ub = to16(cb);
-#pragma unroll 8
-                for (int j = 0; j < min(nr, 32); ++j) copy_row(from16(__shfl_sync(0xffffffffu, ua, j)), r0 + j);
-                if (kWarpRows > 32)
-                    for (int j = 32; j < nr; ++j) copy_row(from16(__shfl_sync(0xffffffffu, ub, j - 32)), r0 + j);
-            } else {
-#pragma unroll 4
-                for (int j = 0; j < min(nr, 32); ++j) copy_row(__shfl_sync(0xffffffffu, ca, j), r0 + j);
-                if (kWarpRows > 32)
-                    for (int j = 32; j < nr; ++j) copy_row(__shfl_sync(0xffffffffu, cb, j - 32), r0 + j);
+            // Branch-free copies: a row without a token (offset < 0) is zero-filled by a
+            // source size of 0, nothing being read for it.
+#pragma unroll
+            for (int g = 0; g < kWarpGroupsMax; ++g) {
+                if (g < ng) {
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) {
+                        const int j = 8 * g + jj;
+                        const long long o = __shfl_sync(0xffffffffu, j < 32 ? ca : cb, j & 31);
+                        const uint32_t d = g * kGroupBytes + jj * 128 + ((lx ^ jj) << 4);
+                        const bool ok = o >= 0;
+                        const uint64_t src = ok ? static_cast<uint64_t>(o) : 0;
+                        cp_async_16_zfill(kdst + d, kbase + src, ok ? 16u : 0u);
+                        if (!p.kv_same) cp_async_16_zfill(vdst + d, vbase + src, ok ? 16u : 0u);
+                    }
+                }
             }
             // One arrival per lane, made when the lane's copies so far have landed (.noinc: the
             // arrival counts toward the barrier's expected 96 per tile).
