@@ -58,8 +58,18 @@ constexpr int kProducerWarps = 3;
 constexpr int kMmaWarp = 3;
 constexpr int kSoftmaxWarp0 = 4;
 constexpr int kSoftmaxWarps = 8;
-constexpr int kThreads = (kSoftmaxWarp0 + kSoftmaxWarps) * 32;  // 384: 3 warps per SM sub-partition
+constexpr int kCorrWarp0 = kSoftmaxWarp0 + kSoftmaxWarps;  // 12: O rescale, one warp per TMEM lane quarter
+constexpr int kCorrWarps = 4;
+constexpr int kThreads = (kCorrWarp0 + kCorrWarps) * 32;  // 512: four warpgroups
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
+// Registers per thread: the block is launched with kLaunchRegs per thread (the most that
+// 512 threads may hold); the softmax warpgroups then take kRegsHigh and the other two
+// warpgroups (gather + MMA, correction) give theirs down to kRegsLow. The split must add
+// up to the launch total exactly, or a warpgroup's increase would wait forever.
+constexpr int kLaunchRegs = 65536 / kThreads;  // 128
+constexpr int kRegsHigh = 168;
+constexpr int kRegsLow = 88;
+static_assert(2 * 128 * kRegsLow + 2 * 128 * kRegsHigh == kThreads * kLaunchRegs, "register split");
 
 constexpr int kBarSoftmax = 1;  // named barrier over the softmax warps
 
@@ -77,8 +87,9 @@ static_assert(kSlotsKV <= 6 && kSBufs >= 1 && kScores % 16 == 0, "tile geometry"
 constexpr int kOffRing = 0;
 constexpr int kOffP = kOffRing + kRingBytes;                     // P' [2 buffers][hi, lo]; epilogue staging
 constexpr int kOffHm = kOffP + 4 * kPTermBytes;                  // float [2 token halves][64] tile maxima
-constexpr int kOffAlpha = kOffHm + 2 * kHeadsPerCta * 4;         // float [64] rescale factors
-constexpr int kOffL = kOffAlpha + kHeadsPerCta * 4;              // float [2 token halves][64] row sums
+constexpr int kOffAlpha = kOffHm + 2 * kHeadsPerCta * 4;         // float [2 tiles][64] rescale factors
+constexpr int kOffResc = kOffAlpha + 2 * kHeadsPerCta * 4;       // int [2 tiles]: 32-head blocks to rescale
+constexpr int kOffL = kOffResc + 16;                             // float [2 token halves][64] row sums
 constexpr int kOffF = kOffL + 2 * kHeadsPerCta * 4;              // float [64] output factors
 constexpr int kOffBars = kOffF + kHeadsPerCta * 4;
 enum {
@@ -88,7 +99,9 @@ enum {
     BAR_SEMPTY0 = 14, // 2: S buffer read by the softmax warps
     BAR_PFULL0 = 16,  // 2: P buffer written
     BAR_PVDONE0 = BAR_PFULL0 + 2,  // 2: the P.V reading a P buffer is done
-    BAR_QFULL = BAR_PVDONE0 + 2,
+    BAR_ALPHA0 = BAR_PVDONE0 + 2,  // 2: a tile's rescale factors published by the softmax warps
+    BAR_OCORR0 = BAR_ALPHA0 + 2,   // 2: O rescaled (or left alone) for a tile by the correction warps
+    BAR_QFULL = BAR_OCORR0 + 2,
     BAR_QEMPTY,
     BAR_OEMPTY,
     BAR_DRAIN,
@@ -364,8 +377,8 @@ __device__ void run_producer_tma(const DecodeParams& p, const CUtensorMap* kmap,
 __device__ __forceinline__ bool warp_poll(uint32_t bar, uint32_t parity) {
     return __all_sync(0xffffffffu, mbar_try_wait(bar, parity) != 0);
 }
-// Slow path of mma_wait, out of line (see mbar_wait).
-static __device__ __noinline__ void mma_wait_slow(const DecodeParams& p, uint32_t bar, uint32_t parity,
+// Slow path of mma_wait (polling until the phase completes or the limit passes).
+__device__ __forceinline__ void mma_wait_slow(const DecodeParams& p, uint32_t bar, uint32_t parity,
                                            volatile int* abort_flag) {
     if (p.wait_limit_ns < kPollHintNs) {  // below the polling interval: the test has failed
         fail(p, abort_flag, kStatusTimeout);
@@ -407,6 +420,7 @@ __device__ void run_mma(const DecodeParams& p, uint32_t sbase, uint32_t tmem, vo
     auto issue_pv = [&](uint32_t tp, bool first) {
         const int pb = tp & 1;
         mma_wait(p, barp(BAR_PFULL0 + pb), (tp >> 1) & 1, abort_flag);
+        mma_wait(p, barp(BAR_OCORR0 + pb), (tp >> 1) & 1, abort_flag);
         if (first && qseg > 0) mma_wait(p, barp(BAR_OEMPTY), (qseg - 1) & 1, abort_flag);
         tc_fence_after();
         const int e = static_cast<int>(tp % ring.slots);
@@ -475,7 +489,8 @@ __device__ void run_mma(const DecodeParams& p, uint32_t sbase, uint32_t tmem, vo
                     if (t == tl.ntiles - 1) tc_commit_el(barp(BAR_QEMPTY), el);
                     qk_done = true;
                 }
-                if (!pv_done && warp_poll(barp(BAR_PFULL0 + ((tau - 1) & 1)), ((tau - 1) >> 1) & 1)) {
+                if (!pv_done && warp_poll(barp(BAR_PFULL0 + ((tau - 1) & 1)), ((tau - 1) >> 1) & 1) &&
+                    warp_poll(barp(BAR_OCORR0 + ((tau - 1) & 1)), ((tau - 1) >> 1) & 1)) {
                     if (tau - 1 < 8) DSA_TRACE_AT(p, 64 + tau - 1);
                     issue_pv(tau - 1, tau - 1 == tau0);
                     pv_done = true;
@@ -541,6 +556,56 @@ __device__ __forceinline__ void store_block(T* rows, int h0, int hvalid, int dim
     __syncwarp();
 }
 
+// ------------------------------------------------------------------------------------
+// correction warps: O rescale
+// ------------------------------------------------------------------------------------
+// Warp kCorrWarp0 + q owns TMEM lanes 32q..32q+31 (dims 32q.. of every 128-dim chunk). For
+// each tile it takes the softmax warps' factors and, when a 32-head block's reference
+// moved, multiplies that block's O^T columns by them once the previous P.V is done; the
+// tile's P.V waits for this through the correction barrier. The softmax warps meanwhile
+// go on to the next tile.
+__device__ void run_correction(const DecodeParams& p, uint8_t* smem, uint32_t sbase, uint32_t tmem,
+                               volatile int* abort_flag, int nseg, const Segment& seg0) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const float* alpha2_s = reinterpret_cast<const float*>(smem + kOffAlpha);
+    const volatile int* resc_s = reinterpret_cast<const volatile int*>(smem + kOffResc);
+    auto barp = [&](int b) { return sbase + kOffBars + 8 * b; };
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    uint32_t tau = 0;
+    for (int i = 0; i < nseg; ++i) {
+        const Segment s = i == 0 ? seg0 : cta_segment(p.part, blockIdx.x, i);
+        const Tiles tl = segment_tokens(p, s);
+        if (tl.n <= 0) continue;
+        for (int t = 0; t < tl.ntiles; ++t, ++tau) {
+            warp_wait(p, barp(BAR_ALPHA0 + (tau & 1)), (tau >> 1) & 1, abort_flag);
+            const int flags = __shfl_sync(0xffffffffu, resc_s[tau & 1], 0);
+            if (flags != 0) {
+                const float* alpha_s = alpha2_s + (tau & 1) * kHeadsPerCta;
+                warp_wait(p, barp(BAR_PVDONE0 + ((tau - 1) & 1)), ((tau - 1) >> 1) & 1, abort_flag);
+                tc_fence_after();
+#pragma unroll 1
+                for (int mc = 0; mc < 4; ++mc) {
+#pragma unroll 1
+                    for (int hh = 0; hh < 2; ++hh) {
+                        if (!(flags & (1 << hh))) continue;
+                        const uint32_t ta = tmem + lane_base + kTmemO + mc * 64 + hh * 32;
+                        uint32_t o[32];
+                        tmem_ld_x32(ta, o);
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha_s[hh * 32 + k]);
+                        tmem_st_x32(ta, o);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(barp(BAR_OCORR0 + (tau & 1)));
+        }
+    }
+}
+
 __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase, uint32_t tmem,
                             volatile int* abort_flag, int nseg, const Segment& seg0) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -551,7 +616,8 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
     const int hq = 16 * q4 + (lane >> 1);     // head of this thread within the unit
     const int st = sw * 32 + lane;            // 0..255
     float* hm_s = reinterpret_cast<float*>(smem + kOffHm);
-    float* alpha_s = reinterpret_cast<float*>(smem + kOffAlpha);
+    float* alpha2_s = reinterpret_cast<float*>(smem + kOffAlpha);  // [2 tiles][64]
+    int* resc_s = reinterpret_cast<int*>(smem + kOffResc);
     float* l_s = reinterpret_cast<float*>(smem + kOffL);
     float* f_s = reinterpret_cast<float*>(smem + kOffF);
     static_assert(kSoftmaxWarps * 2048 <= 4 * kPTermBytes, "epilogue staging fits the P buffers");
@@ -656,8 +722,14 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
             const bool under = hmax < m_ref - kRescaleDrop && m_ref > m_top - kRescaleFloor;
             const bool any_change = named_bar_any<kBarSoftmax, kSoftmaxThreads>(over || under);
             if (st == 0 && (tau == 2 || tau == 3)) DSA_TRACE_AT(p, 73 + 8 * (tau - 2));
-            // 32-head blocks of O^T that need rescaling before this tile's P.V (uniform).
+            // 32-head blocks of O^T that need rescaling before this tile's P.V (uniform); the
+            // correction warps do the rescaling with this tile's factors.
             bool resc[2] = {false, false};
+            float* alpha_s = alpha2_s + (tau & 1) * kHeadsPerCta;
+            // This tile's P buffer, factor buffer and flag word were last used by tile tau - 2:
+            // its P.V has read the P buffer, and its correction (done before that P.V could
+            // start) has read the factors and the flags.
+            if (tau >= 2) warp_wait(p, barp(BAR_PVDONE0 + (tau & 1)), ((tau >> 1) - 1) & 1, abort_flag);
             if (any_change) {
                 // Reset the reference of every head whose tile max exceeds it by more than
                 // the margin, or lies more than kRescaleDrop below it; O and the row sums
@@ -689,6 +761,9 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
                     }
                 }
             }
+            if (st == 0) resc_s[tau & 1] = (resc[0] ? 1 : 0) | (resc[1] ? 2 : 0);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(barp(BAR_ALPHA0 + (tau & 1)));
 
             // P' = 2^(x - m + kPBias) as two E4M3 terms, 16 tokens per 16-byte row.
             uint32_t hw[kScores / 4], lw[kScores / 4];
@@ -709,8 +784,6 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
             }
             l_part += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
             if (st == 0 && (tau == 2 || tau == 3)) DSA_TRACE_AT(p, 74 + 8 * (tau - 2));
-            // P buffer tau%2 is free once the P.V two tiles back has finished reading it.
-            if (tau >= 2) warp_wait(p, barp(BAR_PVDONE0 + (tau & 1)), ((tau >> 1) - 1) & 1, abort_flag);
             if (st == 0 && (tau == 2 || tau == 3)) DSA_TRACE_AT(p, 75 + 8 * (tau - 2));
             const uint32_t pb = sbase + kOffP + (tau & 1) * 2 * kPTermBytes;
 #pragma unroll
@@ -719,29 +792,6 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
                 st_shared_v4(pb + kPTermBytes + p_off + c * 1024, lw[4 * c], lw[4 * c + 1], lw[4 * c + 2], lw[4 * c + 3]);
             }
             fence_proxy_async_smem();
-            if (resc[0] || resc[1]) {
-                // O^T columns are heads: this warp rescales its lanes of chunks 2*half and
-                // 2*half + 1 once the P.V before this tile is done. Doing it after the P
-                // write lets that P.V run while this tile's probabilities are formed; this
-                // tile's P.V waits for the rescale through the P-full barrier below.
-                warp_wait(p, barp(BAR_PVDONE0 + ((tau - 1) & 1)), ((tau - 1) >> 1) & 1, abort_flag);
-                tc_fence_after();
-#pragma unroll 1
-                for (int mc2 = 0; mc2 < 2; ++mc2) {
-#pragma unroll 1
-                    for (int hh = 0; hh < 2; ++hh) {
-                        if (!resc[hh]) continue;
-                        const uint32_t ta = tmem + lane_base + kTmemO + (2 * half + mc2) * 64 + hh * 32;
-                        uint32_t o[32];
-                        tmem_ld_x32(ta, o);
-#pragma unroll
-                        for (int k = 0; k < 32; ++k)
-                            o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha_s[hh * 32 + k]);
-                        tmem_st_x32(ta, o);
-                    }
-                }
-                tmem_wait_st();
-            }
             if (st == 0 && (tau == 2 || tau == 3)) DSA_TRACE_AT(p, 76 + 8 * (tau - 2));
             tc_fence_before();
             __syncwarp();
@@ -836,6 +886,8 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p, const CUtenso
         for (int k = 0; k < 2; ++k) {
             mbar_init(b + 8 * (BAR_PFULL0 + k), kSoftmaxWarps);
             mbar_init(b + 8 * (BAR_PVDONE0 + k), 1);
+            mbar_init(b + 8 * (BAR_ALPHA0 + k), kSoftmaxWarps);
+            mbar_init(b + 8 * (BAR_OCORR0 + k), kCorrWarps);
         }
         mbar_init(b + 8 * BAR_QFULL, kSoftmaxWarps);
         mbar_init(b + 8 * BAR_QEMPTY, 1);
@@ -871,31 +923,41 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p, const CUtenso
     // (it waits for this grid's completion before reading its results); short ones at the end.
     if (p.early_dependents) griddep_launch_dependents();
 
-    if (warp < kProducerWarps) {
-        if constexpr (!kTma)
-            run_producer(p, sbase, abort_flag, nseg, seg0);
-        else if (warp == 0)
-            run_producer_tma(p, kmap, vmap, sbase, abort_flag, nseg, seg0);
-    } else if (warp == kMmaWarp) {
-        run_mma(p, sbase, tmem, abort_flag, nseg, seg0);
-        // Wait (bounded, regardless of abort) until every issued MMA has completed and the
-        // softmax warps have finished reading TMEM.
-        const uint32_t db = sbase + kOffBars + 8 * BAR_DRAIN;
-        tc_commit_el(db, elect_one());
-        uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(db, 0) && globaltimer_ns() - t0 < kDrainLimitNs) {
+    // Registers move from the gather/MMA and correction warpgroups to the softmax warpgroups
+    // (see kRegsHigh). Each role's branch starts with its warpgroup's setmaxnreg, which
+    // every warp of the warpgroup executes.
+    if (warp < kSoftmaxWarp0) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+        if (warp < kProducerWarps) {
+            if constexpr (!kTma)
+                run_producer(p, sbase, abort_flag, nseg, seg0);
+            else if (warp == 0)
+                run_producer_tma(p, kmap, vmap, sbase, abort_flag, nseg, seg0);
+        } else {
+            run_mma(p, sbase, tmem, abort_flag, nseg, seg0);
+            // Wait (bounded, regardless of abort) until every issued MMA has completed and the
+            // softmax warps have finished reading TMEM.
+            const uint32_t db = sbase + kOffBars + 8 * BAR_DRAIN;
+            tc_commit_el(db, elect_one());
+            uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(db, 0) && globaltimer_ns() - t0 < kDrainLimitNs) {
+            }
+            DSA_TRACE_AT(p, 11);
+            const uint32_t done = sbase + kOffBars + 8 * BAR_DONE;
+            t0 = globaltimer_ns();
+            while (!mbar_try_wait(done, 0) && globaltimer_ns() - t0 < kDrainLimitNs) {
+            }
+            __syncwarp();
         }
-        DSA_TRACE_AT(p, 11);
-        const uint32_t done = sbase + kOffBars + 8 * BAR_DONE;
-        t0 = globaltimer_ns();
-        while (!mbar_try_wait(done, 0) && globaltimer_ns() - t0 < kDrainLimitNs) {
-        }
-        __syncwarp();
-    } else {
+    } else if (warp < kCorrWarp0) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
         run_softmax(p, smem, sbase, tmem, abort_flag, nseg, seg0);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(sbase + kOffBars + 8 * BAR_DONE);
+    } else {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+        run_correction(p, smem, sbase, tmem, abort_flag, nseg, seg0);
     }
     tc_fence_before();
     __syncthreads();
@@ -928,6 +990,9 @@ cudaError_t setup_instance(K kernel) {
     cudaError_t e = cudaFuncGetAttributes(&attr, kernel);
     if (e != cudaSuccess) return e;
     if (attr.maxThreadsPerBlock < kThreads) return cudaErrorInvalidConfiguration;
+    // The register split assumes the block starts with exactly kLaunchRegs per thread; with
+    // any other count a warpgroup's increase could wait forever, so the kernel is refused.
+    if (attr.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);

@@ -87,10 +87,10 @@ constexpr uint32_t kPollHintNs = 500;
 // The suspend hint never exceeds the limit, so a short limit is not hidden by a long
 // suspension that the phase happens to end. A limit below kPollHintNs (finer than the
 // polling interval, and than %globaltimer's steps may be) makes the wait a single
-// non-blocking test: it gives up at once when the phase is not complete. The polling loop
-// is kept out of line: waits sit at many places in the kernel and its warps share one
-// instruction cache.
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const volatile int* abort_flag,
+// non-blocking test: it gives up at once when the phase is not complete. (The loop is
+// inlined: kernels that move registers between warpgroups with setmaxnreg cannot call
+// functions.)
+__device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const volatile int* abort_flag,
                                             uint64_t limit_ns) {
     if (limit_ns < kPollHintNs) return false;
     const uint32_t hint = limit_ns < kSuspendHintNs ? static_cast<uint32_t>(limit_ns) : kSuspendHintNs;
