@@ -58,18 +58,8 @@ constexpr int kProducerWarps = 3;
 constexpr int kMmaWarp = 3;
 constexpr int kSoftmaxWarp0 = 4;
 constexpr int kSoftmaxWarps = 8;
-constexpr int kCorrWarp0 = kSoftmaxWarp0 + kSoftmaxWarps;  // 12: O rescale, one warp per TMEM lane quarter
-constexpr int kCorrWarps = 4;
-constexpr int kThreads = (kCorrWarp0 + kCorrWarps) * 32;  // 512: four warpgroups
+constexpr int kThreads = (kSoftmaxWarp0 + kSoftmaxWarps) * 32;  // 384: 3 warps per SM sub-partition
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
-// Registers per thread: the block is launched with kLaunchRegs per thread (the most that
-// 512 threads may hold); the softmax warpgroups then take kRegsHigh and the other two
-// warpgroups (gather + MMA, correction) give theirs down to kRegsLow. The split must add
-// up to the launch total exactly, or a warpgroup's increase would wait forever.
-constexpr int kLaunchRegs = 65536 / kThreads;  // 128
-constexpr int kRegsHigh = 168;
-constexpr int kRegsLow = 88;
-static_assert(2 * 128 * kRegsLow + 2 * 128 * kRegsHigh == kThreads * kLaunchRegs, "register split");
 
 constexpr int kBarSoftmax = 1;  // named barrier over the softmax warps
 
@@ -87,9 +77,8 @@ static_assert(kSlotsKV <= 6 && kSBufs >= 1 && kScores % 16 == 0, "tile geometry"
 constexpr int kOffRing = 0;
 constexpr int kOffP = kOffRing + kRingBytes;                     // P' [2 buffers][hi, lo]; epilogue staging
 constexpr int kOffHm = kOffP + 4 * kPTermBytes;                  // float [2 token halves][64] tile maxima
-constexpr int kOffAlpha = kOffHm + 2 * kHeadsPerCta * 4;         // float [2 tiles][64] rescale factors
-constexpr int kOffResc = kOffAlpha + 2 * kHeadsPerCta * 4;       // int [2 tiles]: 32-head blocks to rescale
-constexpr int kOffL = kOffResc + 16;                             // float [2 token halves][64] row sums
+constexpr int kOffAlpha = kOffHm + 2 * kHeadsPerCta * 4;         // float [64] rescale factors
+constexpr int kOffL = kOffAlpha + kHeadsPerCta * 4;              // float [2 token halves][64] row sums
 constexpr int kOffF = kOffL + 2 * kHeadsPerCta * 4;              // float [64] output factors
 constexpr int kOffBars = kOffF + kHeadsPerCta * 4;
 enum {
@@ -99,9 +88,7 @@ enum {
     BAR_SEMPTY0 = 14, // 2: S buffer read by the softmax warps
     BAR_PFULL0 = 16,  // 2: P buffer written
     BAR_PVDONE0 = BAR_PFULL0 + 2,  // 2: the P.V reading a P buffer is done
-    BAR_ALPHA0 = BAR_PVDONE0 + 2,  // 2: a tile's rescale factors published by the softmax warps
-    BAR_OCORR0 = BAR_ALPHA0 + 2,   // 2: O rescaled (or left alone) for a tile by the correction warps
-    BAR_QFULL = BAR_OCORR0 + 2,
+    BAR_QFULL = BAR_PVDONE0 + 2,
     BAR_QEMPTY,
     BAR_OEMPTY,
     BAR_DRAIN,
@@ -195,28 +182,16 @@ struct Ring {
 // ------------------------------------------------------------------------------------
 // gather warps
 // ------------------------------------------------------------------------------------
-// The tile's rows are dealt out in groups of 8 (one swizzle group each): warp w takes
-// groups [g0, g0 + ng), 6/5/5 groups for 128-token tiles and 3/3/2 for 64-token tiles.
-// Every warp's rows then start at a multiple of 8, so within a group the swizzle term of a
-// row depends only on the lane and the row's compile-time index: a row costs one shuffle
-// of its offset, one address add and one cp.async.
-constexpr int kGroups8 = kTileTokens / 8;
-constexpr int kWarpGroupsMax = (kGroups8 + kProducerWarps - 1) / kProducerWarps;
-static_assert(kWarpGroupsMax * 8 <= 64, "a warp's rows fit two offsets per lane");
+// Rows of a tile taken by gather warp w: [w*43, min(w*43 + 43, 128)).
+constexpr int kWarpRows = (kTileTokens + kProducerWarps - 1) / kProducerWarps;
 
 __device__ void run_producer(const DecodeParams& p, uint32_t sbase, volatile int* abort_flag, int nseg,
                              const Segment& seg0) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const Ring ring(p.kv_same);
     const int64_t W = p.part.width;
-    const int ng = kGroups8 / kProducerWarps + (warp < kGroups8 % kProducerWarps ? 1 : 0);
-    const int g0 = warp * (kGroups8 / kProducerWarps) + min(warp, kGroups8 % kProducerWarps);
-    const int r0 = 8 * g0;
-    const int nr = 8 * ng;
-    const uint32_t lane_dst = static_cast<uint32_t>(g0) * kGroupBytes + (lane >> 3) * 1024;
-    const uint32_t lx = lane & 7;
-    const uint8_t* kbase = p.k_cache + lane * 16;
-    const uint8_t* vbase = p.v_cache + lane * 16;
+    const int r0 = warp * kWarpRows;
+    const int nr = min(kWarpRows, kTileTokens - r0);
     uint32_t tau = 0;
     if (tid == 0) DSA_TRACE_AT(p, 2);
     for (int i = 0; i < nseg; ++i) {
@@ -243,7 +218,7 @@ __device__ void run_producer(const DecodeParams& p, uint32_t sbase, volatile int
         for (int t = 0; t < tl.ntiles; ++t, ++tau) {
             const long long ca = oa, cb = ob;
             if (tid == 0 && t == 0 && i == 0 && ca != 12345) DSA_TRACE_AT(p, 5);
-            load(t + 1, oa, ob);  // next tile's offsets, before the slot wait
+            load(t + 1, oa, ob);  // next tile's rows, before the slot wait
             if (tid == 0 && t == 0 && i == 0) DSA_TRACE_AT(p, 6);
             if ((ca < 0 && t * kTileTokens + r0 + lane < tl.n) ||
                 (cb < 0 && lane + 32 < nr && t * kTileTokens + r0 + 32 + lane < tl.n))
@@ -254,24 +229,37 @@ __device__ void run_producer(const DecodeParams& p, uint32_t sbase, volatile int
             if (tau >= static_cast<uint32_t>(ring.slots))
                 warp_wait(p, sbase + kOffBars + 8 * (BAR_EMPTY0 + e), (use - 1) & 1, abort_flag);
             if (tid == 0 && tau < 8) DSA_TRACE_AT(p, 40 + tau);
-            const uint32_t kdst = sbase + kOffRing + e * ring.slot_bytes + lane_dst;
+            const uint32_t kdst = sbase + kOffRing + e * ring.slot_bytes;
             const uint32_t vdst = kdst + kKvTileBytes;
-            // Branch-free copies: a row without a token (offset < 0) is zero-filled by a
-            // source size of 0, nothing being read for it.
-#pragma unroll
-            for (int g = 0; g < kWarpGroupsMax; ++g) {
-                if (g < ng) {
-#pragma unroll
-                    for (int jj = 0; jj < 8; ++jj) {
-                        const int j = 8 * g + jj;
-                        const long long o = __shfl_sync(0xffffffffu, j < 32 ? ca : cb, j & 31);
-                        const uint32_t d = g * kGroupBytes + jj * 128 + ((lx ^ jj) << 4);
-                        const bool ok = o >= 0;
-                        const uint64_t src = ok ? static_cast<uint64_t>(o) : 0;
-                        cp_async_16_zfill(kdst + d, kbase + src, ok ? 16u : 0u);
-                        if (!p.kv_same) cp_async_16_zfill(vdst + d, vbase + src, ok ? 16u : 0u);
-                    }
-                }
+            // Branch-free copy loop (a branch on the shuffled offset would serialise the
+            // copies): rows without a token (o < 0) are zero-filled by a source size of 0.
+            // Each row's offset is broadcast from the lane holding it. Offsets below 64 GiB
+            // travel as 32-bit counts of 16-byte units (one shuffle per row; 0xFFFFFFFF marks
+            // a row without token); a tile with a larger offset takes the 64-bit path.
+            const uint8_t* kbase = p.k_cache + lane * 16;
+            const uint8_t* vbase = p.v_cache + lane * 16;
+            auto copy_row = [&](long long o, int tk) {
+                const uint32_t d = (tk >> 3) * kGroupBytes + (lane >> 3) * 1024 + (tk & 7) * 128 +
+                                   (((lane & 7) ^ (tk & 7)) << 4);
+                const bool ok = o >= 0;
+                const uint64_t src = ok ? static_cast<uint64_t>(o) : 0;
+                cp_async_16_zfill(kdst + d, kbase + src, ok ? 16u : 0u);
+                if (!p.kv_same) cp_async_16_zfill(vdst + d, vbase + src, ok ? 16u : 0u);
+            };
+            constexpr long long kNarrow = 1ll << 36;
+            if (!__any_sync(0xffffffffu, ca >= kNarrow || cb >= kNarrow)) {
+                auto to16 = [](long long o) { return o >= 0 ? static_cast<uint32_t>(o >> 4) : 0xFFFFFFFFu; };
+                auto from16 = [](uint32_t u) { return u != 0xFFFFFFFFu ? static_cast<long long>(u) << 4 : -1ll; };
+                const uint32_t ua = to16(ca), ub = to16(cb);
+#pragma unroll 8
+                for (int j = 0; j < min(nr, 32); ++j) copy_row(from16(__shfl_sync(0xffffffffu, ua, j)), r0 + j);
+                if (kWarpRows > 32)
+                    for (int j = 32; j < nr; ++j) copy_row(from16(__shfl_sync(0xffffffffu, ub, j - 32)), r0 + j);
+            } else {
+#pragma unroll 4
+                for (int j = 0; j < min(nr, 32); ++j) copy_row(__shfl_sync(0xffffffffu, ca, j), r0 + j);
+                if (kWarpRows > 32)
+                    for (int j = 32; j < nr; ++j) copy_row(__shfl_sync(0xffffffffu, cb, j - 32), r0 + j);
             }
             // One arrival per lane, made when the lane's copies so far have landed (.noinc: the
             // arrival counts toward the barrier's expected 96 per tile).
@@ -377,8 +365,8 @@ __device__ void run_producer_tma(const DecodeParams& p, const CUtensorMap* kmap,
 __device__ __forceinline__ bool warp_poll(uint32_t bar, uint32_t parity) {
     return __all_sync(0xffffffffu, mbar_try_wait(bar, parity) != 0);
 }
-// Slow path of mma_wait (polling until the phase completes or the limit passes).
-__device__ __forceinline__ void mma_wait_slow(const DecodeParams& p, uint32_t bar, uint32_t parity,
+// Slow path of mma_wait, out of line (see mbar_wait).
+static __device__ __noinline__ void mma_wait_slow(const DecodeParams& p, uint32_t bar, uint32_t parity,
                                            volatile int* abort_flag) {
     if (p.wait_limit_ns < kPollHintNs) {  // below the polling interval: the test has failed
         fail(p, abort_flag, kStatusTimeout);
@@ -420,7 +408,6 @@ __device__ void run_mma(const DecodeParams& p, uint32_t sbase, uint32_t tmem, vo
     auto issue_pv = [&](uint32_t tp, bool first) {
         const int pb = tp & 1;
         mma_wait(p, barp(BAR_PFULL0 + pb), (tp >> 1) & 1, abort_flag);
-        mma_wait(p, barp(BAR_OCORR0 + pb), (tp >> 1) & 1, abort_flag);
         if (first && qseg > 0) mma_wait(p, barp(BAR_OEMPTY), (qseg - 1) & 1, abort_flag);
         tc_fence_after();
         const int e = static_cast<int>(tp % ring.slots);
@@ -489,8 +476,7 @@ __device__ void run_mma(const DecodeParams& p, uint32_t sbase, uint32_t tmem, vo
                     if (t == tl.ntiles - 1) tc_commit_el(barp(BAR_QEMPTY), el);
                     qk_done = true;
                 }
-                if (!pv_done && warp_poll(barp(BAR_PFULL0 + ((tau - 1) & 1)), ((tau - 1) >> 1) & 1) &&
-                    warp_poll(barp(BAR_OCORR0 + ((tau - 1) & 1)), ((tau - 1) >> 1) & 1)) {
+                if (!pv_done && warp_poll(barp(BAR_PFULL0 + ((tau - 1) & 1)), ((tau - 1) >> 1) & 1)) {
                     if (tau - 1 < 8) DSA_TRACE_AT(p, 64 + tau - 1);
                     issue_pv(tau - 1, tau - 1 == tau0);
                     pv_done = true;
@@ -556,56 +542,6 @@ __device__ __forceinline__ void store_block(T* rows, int h0, int hvalid, int dim
     __syncwarp();
 }
 
-// ------------------------------------------------------------------------------------
-// correction warps: O rescale
-// ------------------------------------------------------------------------------------
-// Warp kCorrWarp0 + q owns TMEM lanes 32q..32q+31 (dims 32q.. of every 128-dim chunk). For
-// each tile it takes the softmax warps' factors and, when a 32-head block's reference
-// moved, multiplies that block's O^T columns by them once the previous P.V is done; the
-// tile's P.V waits for this through the correction barrier. The softmax warps meanwhile
-// go on to the next tile.
-__device__ void run_correction(const DecodeParams& p, uint8_t* smem, uint32_t sbase, uint32_t tmem,
-                               volatile int* abort_flag, int nseg, const Segment& seg0) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const float* alpha2_s = reinterpret_cast<const float*>(smem + kOffAlpha);
-    const volatile int* resc_s = reinterpret_cast<const volatile int*>(smem + kOffResc);
-    auto barp = [&](int b) { return sbase + kOffBars + 8 * b; };
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    uint32_t tau = 0;
-    for (int i = 0; i < nseg; ++i) {
-        const Segment s = i == 0 ? seg0 : cta_segment(p.part, blockIdx.x, i);
-        const Tiles tl = segment_tokens(p, s);
-        if (tl.n <= 0) continue;
-        for (int t = 0; t < tl.ntiles; ++t, ++tau) {
-            warp_wait(p, barp(BAR_ALPHA0 + (tau & 1)), (tau >> 1) & 1, abort_flag);
-            const int flags = __shfl_sync(0xffffffffu, resc_s[tau & 1], 0);
-            if (flags != 0) {
-                const float* alpha_s = alpha2_s + (tau & 1) * kHeadsPerCta;
-                warp_wait(p, barp(BAR_PVDONE0 + ((tau - 1) & 1)), ((tau - 1) >> 1) & 1, abort_flag);
-                tc_fence_after();
-#pragma unroll 1
-                for (int mc = 0; mc < 4; ++mc) {
-#pragma unroll 1
-                    for (int hh = 0; hh < 2; ++hh) {
-                        if (!(flags & (1 << hh))) continue;
-                        const uint32_t ta = tmem + lane_base + kTmemO + mc * 64 + hh * 32;
-                        uint32_t o[32];
-                        tmem_ld_x32(ta, o);
-#pragma unroll
-                        for (int k = 0; k < 32; ++k)
-                            o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha_s[hh * 32 + k]);
-                        tmem_st_x32(ta, o);
-                    }
-                }
-                tmem_wait_st();
-                tc_fence_before();
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(barp(BAR_OCORR0 + (tau & 1)));
-        }
-    }
-}
-
 __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase, uint32_t tmem,
                             volatile int* abort_flag, int nseg, const Segment& seg0) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -616,8 +552,7 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
     const int hq = 16 * q4 + (lane >> 1);     // head of this thread within the unit
     const int st = sw * 32 + lane;            // 0..255
     float* hm_s = reinterpret_cast<float*>(smem + kOffHm);
-    float* alpha2_s = reinterpret_cast<float*>(smem + kOffAlpha);  // [2 tiles][64]
-    int* resc_s = reinterpret_cast<int*>(smem + kOffResc);
+    float* alpha_s = reinterpret_cast<float*>(smem + kOffAlpha);
     float* l_s = reinterpret_cast<float*>(smem + kOffL);
     float* f_s = reinterpret_cast<float*>(smem + kOffF);
     static_assert(kSoftmaxWarps * 2048 <= 4 * kPTermBytes, "epilogue staging fits the P buffers");
@@ -722,14 +657,8 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
             const bool under = hmax < m_ref - kRescaleDrop && m_ref > m_top - kRescaleFloor;
             const bool any_change = named_bar_any<kBarSoftmax, kSoftmaxThreads>(over || under);
             if (st == 0 && (tau == 2 || tau == 3)) DSA_TRACE_AT(p, 73 + 8 * (tau - 2));
-            // 32-head blocks of O^T that need rescaling before this tile's P.V (uniform); the
-            // correction warps do the rescaling with this tile's factors.
+            // 32-head blocks of O^T that need rescaling before this tile's P.V (uniform).
             bool resc[2] = {false, false};
-            float* alpha_s = alpha2_s + (tau & 1) * kHeadsPerCta;
-            // This tile's P buffer, factor buffer and flag word were last used by tile tau - 2:
-            // its P.V has read the P buffer, and its correction (done before that P.V could
-            // start) has read the factors and the flags.
-            if (tau >= 2) warp_wait(p, barp(BAR_PVDONE0 + (tau & 1)), ((tau >> 1) - 1) & 1, abort_flag);
             if (any_change) {
                 // Reset the reference of every head whose tile max exceeds it by more than
                 // the margin, or lies more than kRescaleDrop below it; O and the row sums
@@ -761,9 +690,6 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
                     }
                 }
             }
-            if (st == 0) resc_s[tau & 1] = (resc[0] ? 1 : 0) | (resc[1] ? 2 : 0);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(barp(BAR_ALPHA0 + (tau & 1)));
 
             // P' = 2^(x - m + kPBias) as two E4M3 terms, 16 tokens per 16-byte row.
             uint32_t hw[kScores / 4], lw[kScores / 4];
@@ -784,6 +710,8 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
             }
             l_part += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
             if (st == 0 && (tau == 2 || tau == 3)) DSA_TRACE_AT(p, 74 + 8 * (tau - 2));
+            // P buffer tau%2 is free once the P.V two tiles back has finished reading it.
+            if (tau >= 2) warp_wait(p, barp(BAR_PVDONE0 + (tau & 1)), ((tau >> 1) - 1) & 1, abort_flag);
             if (st == 0 && (tau == 2 || tau == 3)) DSA_TRACE_AT(p, 75 + 8 * (tau - 2));
             const uint32_t pb = sbase + kOffP + (tau & 1) * 2 * kPTermBytes;
 #pragma unroll
@@ -792,6 +720,29 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
                 st_shared_v4(pb + kPTermBytes + p_off + c * 1024, lw[4 * c], lw[4 * c + 1], lw[4 * c + 2], lw[4 * c + 3]);
             }
             fence_proxy_async_smem();
+            if (resc[0] || resc[1]) {
+                // O^T columns are heads: this warp rescales its lanes of chunks 2*half and
+                // 2*half + 1 once the P.V before this tile is done. Doing it after the P
+                // write lets that P.V run while this tile's probabilities are formed; this
+                // tile's P.V waits for the rescale through the P-full barrier below.
+                warp_wait(p, barp(BAR_PVDONE0 + ((tau - 1) & 1)), ((tau - 1) >> 1) & 1, abort_flag);
+                tc_fence_after();
+#pragma unroll 1
+                for (int mc2 = 0; mc2 < 2; ++mc2) {
+#pragma unroll 1
+                    for (int hh = 0; hh < 2; ++hh) {
+                        if (!resc[hh]) continue;
+                        const uint32_t ta = tmem + lane_base + kTmemO + (2 * half + mc2) * 64 + hh * 32;
+                        uint32_t o[32];
+                        tmem_ld_x32(ta, o);
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha_s[hh * 32 + k]);
+                        tmem_st_x32(ta, o);
+                    }
+                }
+                tmem_wait_st();
+            }
             if (st == 0 && (tau == 2 || tau == 3)) DSA_TRACE_AT(p, 76 + 8 * (tau - 2));
             tc_fence_before();
             __syncwarp();
@@ -886,8 +837,6 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p, const CUtenso
         for (int k = 0; k < 2; ++k) {
             mbar_init(b + 8 * (BAR_PFULL0 + k), kSoftmaxWarps);
             mbar_init(b + 8 * (BAR_PVDONE0 + k), 1);
-            mbar_init(b + 8 * (BAR_ALPHA0 + k), kSoftmaxWarps);
-            mbar_init(b + 8 * (BAR_OCORR0 + k), kCorrWarps);
         }
         mbar_init(b + 8 * BAR_QFULL, kSoftmaxWarps);
         mbar_init(b + 8 * BAR_QEMPTY, 1);
@@ -923,41 +872,31 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p, const CUtenso
     // (it waits for this grid's completion before reading its results); short ones at the end.
     if (p.early_dependents) griddep_launch_dependents();
 
-    // Registers move from the gather/MMA and correction warpgroups to the softmax warpgroups
-    // (see kRegsHigh). Each role's branch starts with its warpgroup's setmaxnreg, which
-    // every warp of the warpgroup executes.
-    if (warp < kSoftmaxWarp0) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
-        if (warp < kProducerWarps) {
-            if constexpr (!kTma)
-                run_producer(p, sbase, abort_flag, nseg, seg0);
-            else if (warp == 0)
-                run_producer_tma(p, kmap, vmap, sbase, abort_flag, nseg, seg0);
-        } else {
-            run_mma(p, sbase, tmem, abort_flag, nseg, seg0);
-            // Wait (bounded, regardless of abort) until every issued MMA has completed and the
-            // softmax warps have finished reading TMEM.
-            const uint32_t db = sbase + kOffBars + 8 * BAR_DRAIN;
-            tc_commit_el(db, elect_one());
-            uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(db, 0) && globaltimer_ns() - t0 < kDrainLimitNs) {
-            }
-            DSA_TRACE_AT(p, 11);
-            const uint32_t done = sbase + kOffBars + 8 * BAR_DONE;
-            t0 = globaltimer_ns();
-            while (!mbar_try_wait(done, 0) && globaltimer_ns() - t0 < kDrainLimitNs) {
-            }
-            __syncwarp();
+    if (warp < kProducerWarps) {
+        if constexpr (!kTma)
+            run_producer(p, sbase, abort_flag, nseg, seg0);
+        else if (warp == 0)
+            run_producer_tma(p, kmap, vmap, sbase, abort_flag, nseg, seg0);
+    } else if (warp == kMmaWarp) {
+        run_mma(p, sbase, tmem, abort_flag, nseg, seg0);
+        // Wait (bounded, regardless of abort) until every issued MMA has completed and the
+        // softmax warps have finished reading TMEM.
+        const uint32_t db = sbase + kOffBars + 8 * BAR_DRAIN;
+        tc_commit_el(db, elect_one());
+        uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(db, 0) && globaltimer_ns() - t0 < kDrainLimitNs) {
         }
-    } else if (warp < kCorrWarp0) {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
+        DSA_TRACE_AT(p, 11);
+        const uint32_t done = sbase + kOffBars + 8 * BAR_DONE;
+        t0 = globaltimer_ns();
+        while (!mbar_try_wait(done, 0) && globaltimer_ns() - t0 < kDrainLimitNs) {
+        }
+        __syncwarp();
+    } else {
         run_softmax(p, smem, sbase, tmem, abort_flag, nseg, seg0);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(sbase + kOffBars + 8 * BAR_DONE);
-    } else {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
-        run_correction(p, smem, sbase, tmem, abort_flag, nseg, seg0);
     }
     tc_fence_before();
     __syncthreads();
@@ -990,9 +929,6 @@ cudaError_t setup_instance(K kernel) {
     cudaError_t e = cudaFuncGetAttributes(&attr, kernel);
     if (e != cudaSuccess) return e;
     if (attr.maxThreadsPerBlock < kThreads) return cudaErrorInvalidConfiguration;
-    // The register split assumes the block starts with exactly kLaunchRegs per thread; with
-    // any other count a warpgroup's increase could wait forever, so the kernel is refused.
-    if (attr.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
