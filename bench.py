@@ -329,7 +329,7 @@ def run_cuda(args, ws_n, rank, local):
                  peak_src == "measured" else "fallback (6.8 TB/s, 1.9 PFLOP/s)",
                  "kernel": "decode_kernel", "kernel_us": round(kernel_us, 3),
                  "step_roofline_us": round(roof_us, 3), "step_frac": round(roof_us / us_per_step, 4)})
-    n_launch = launches_per_step(w0, args.ctas)
+    launches_per_step = 3 if needs_combine(api, w0, args.ctas) else 2
     line = {
         "metric": METRIC, "value": round(us_per_step, 3), "unit": UNIT, "n_gpus": ws_n, "steps": K,
         "warmup": W, "ms_per_step": round(us_per_step / 1e3, 6), "higher_is_better": False,
@@ -337,7 +337,7 @@ def run_cuda(args, ws_n, rank, local):
         "effective_tbs": round(ws_n * cost["bytes"] / (us_per_step * 1e-6) / 1e12, 4),
         "config": config_dict(w0, cost, n_rep, g, ws_n),
         "roofline": roof,
-        "gpu_launches": K * n_launch,
+        "gpu_launches": K * launches_per_step,
         "clocks": clocks,
         "e2e": e2e,
     }
@@ -355,24 +355,14 @@ def config_dict(w: wl.Workload, cost: dict, n_rep: int, graph_steps: int, ws_n: 
             "parallelism": f"replicas x{ws_n}" if ws_n > 1 else "1 GPU"}
 
 
-def launches_per_step(w, ctas) -> int:
-    """Kernels one decode call launches: the prologue and the decode, plus the combine when
-    some unit is split across more than four CTA ranges (up to four, the decode kernel
-    merges the pieces itself). Mirrors the library's static partition."""
+def needs_combine(api, w, ctas) -> bool:
+    # The combine runs when some CTA boundary of the slot partition falls inside a unit.
     groups = (w.num_q_heads + 63) // 64
-    W = w.sel_width
-    T = w.rows * groups * W
+    T = w.rows * groups * w.sel_width
     if ctas <= 0:
         sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
         ctas = max(1, min(sms, (T + 127) // 128))
-    if not any((k * T // ctas) % W != 0 for k in range(1, ctas)):
-        return 2
-
-    def cta_of_slot(x):
-        return ((x + 1) * ctas - 1) // T
-
-    pieces = max(cta_of_slot(u * W + W - 1) - cta_of_slot(u * W) + 1 for u in range(T // W))
-    return 2 if pieces <= 4 else 3
+    return any((k * T // ctas) % w.sel_width != 0 for k in range(1, ctas))
 
 
 def run_e2e(api, reps, args, device, ws_n):

@@ -108,7 +108,6 @@ struct Plan {
     int64_t rows, groups, units;
     Partition part;
     bool any_split;
-    bool fused_combine;  // split units merged inside the decode kernel (few pieces per unit)
     bool small_tiles;  // 64-token tiles: at most two 128-slot tiles of work per CTA
     int max_pieces;    // most CTAs sharing one unit (selects the combine variant)
     WsLayout ws;
@@ -164,7 +163,6 @@ Plan make_plan(int64_t rows, int32_t heads, int32_t width, int32_t num_ctas, int
     for (int64_t k = 1; k < c && !pl.any_split; ++k)
         if (cta_begin(pl.part, k) % width != 0) pl.any_split = true;
     pl.max_pieces = static_cast<int>(std::min<int64_t>(max_pieces_per_unit(pl.part), 1 << 20));
-    pl.fused_combine = pl.any_split && pl.max_pieces <= kFusedMaxPieces;
     pl.ws = ws_layout(rows, pl.groups, width, c);
     return pl;
 }
@@ -218,7 +216,6 @@ int32_t enqueue(const Args& a, const Plan& pl, uint8_t* ws, const CallOptions& o
     pp.cnt = reinterpret_cast<int32_t*>(ws + pl.ws.cnt);
     pp.qimg = ws + pl.ws.qimg;
     pp.qscale = reinterpret_cast<float*>(ws + pl.ws.qscale);
-    pp.arrivals = reinterpret_cast<int*>(ws + pl.ws.arrivals);
     pp.status = reinterpret_cast<int*>(ws + pl.ws.status);
     pp.rows = static_cast<int32_t>(pl.rows);
     pp.width = a.width;
@@ -247,8 +244,6 @@ int32_t enqueue(const Args& a, const Plan& pl, uint8_t* ws, const CallOptions& o
     dp.kv_same = a.k_cache == a.v_cache ? 1 : 0;
     dp.v_scale = a.v_scale;
     dp.early_dependents = early ? 1 : 0;
-    dp.fused_combine = pl.fused_combine ? 1 : 0;
-    dp.arrivals = pp.arrivals;
     dp.wait_limit_ns = opt.wait_limit_ns;
     // Tensor-map gathers (on request) need rows of one uniform stride (dense pages) and
     // 128-byte aligned caches; anything else takes the per-thread copies.
@@ -276,7 +271,7 @@ int32_t enqueue(const Args& a, const Plan& pl, uint8_t* ws, const CallOptions& o
     if (st != DSA_OK) return st;
     if (ev1 && cudaEventRecordWithFlags(ev1, stream, ev_flags) != cudaSuccess) return DSA_ERR_CUDA;
 
-    if (pl.any_split && !pl.fused_combine) {
+    if (pl.any_split) {
         CombineParams cp{};
         cp.part_o = dp.part_o;
         cp.part_lse = dp.part_lse;

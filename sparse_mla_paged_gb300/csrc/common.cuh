@@ -46,7 +46,7 @@ constexpr int kStatusTimeout = DSA_ERR_TIMEOUT;
 // Workspace layout (all offsets 256-byte aligned).
 // ------------------------------------------------------------------------------------
 struct WsLayout {
-    size_t status, offs, cnt, qimg, qscale, part_o, part_lse, arrivals, total;
+    size_t status, offs, cnt, qimg, qscale, part_o, part_lse, total;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -61,7 +61,6 @@ __host__ __device__ inline WsLayout ws_layout(int64_t rows, int64_t groups, int6
     L.qscale = o; o = align256(o + static_cast<size_t>(rows * groups) * kHeadsPerCta * 4);
     L.part_o = o; o = align256(o + static_cast<size_t>(2 * ctas) * kHeadsPerCta * kLatent * 2);
     L.part_lse = o; o = align256(o + static_cast<size_t>(2 * ctas) * kHeadsPerCta * 4);
-    L.arrivals = o; o = align256(o + static_cast<size_t>(rows * groups) * 4);
     L.total = o;
     return L;
 }
@@ -122,10 +121,6 @@ __host__ __device__ inline Segment cta_segment(const Partition& p, int64_t c, in
     return s;
 }
 
-// Most pieces a unit may have for its split to be merged inside the decode kernel (by the
-// last CTA to finish one); units with more are merged by the combine kernel.
-constexpr int kFusedMaxPieces = 4;
-
 // Largest number of CTA ranges that one unit meets (CTAs with an empty range inside the
 // unit included, as the combine kernel walks them): pieces(u) = cta_of_slot(u*W + W - 1) -
 // cta_of_slot(u*W) + 1. A unit met by two or more ranges holds the start of one of them,
@@ -159,7 +154,6 @@ struct PrologueParams {
     int32_t* cnt;              // [R]
     uint8_t* qimg;             // [R*G, 64 KB]
     float* qscale;             // [R*G, 64]
-    int* arrivals;             // [R*G] piece counters of the fused combine, zeroed here (may be null)
     int* status;               // reset by block 0 (may be null)
     int64_t cache_stride;
     int32_t rows, width, heads, groups, rows_per_seq, verify_rows;
@@ -183,10 +177,6 @@ struct DecodeParams {
     int32_t kv_same;
     float v_scale;
     int32_t early_dependents;  // let the next kernel launch once every CTA has started
-    // Split units are merged by the last CTA to finish a piece of them (no combine
-    // launch); arrivals[unit] counts the pieces written so far.
-    int32_t fused_combine;
-    int* arrivals;
     uint64_t wait_limit_ns;    // time limit of each pipeline wait (DSA_ERR_TIMEOUT past it)
     int32_t use_tma;           // gather by tensor map (dense pages), else per-thread copies
     unsigned long long* trace;  // per-CTA timeline, used only by -DDSA_TRACE builds

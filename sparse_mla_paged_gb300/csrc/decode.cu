@@ -97,8 +97,7 @@ enum {
 };
 constexpr int kOffTmemSlot = kOffBars + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
-constexpr int kOffMergeFlag = kOffAbort + 4;
-constexpr int kSmemUsed = kOffMergeFlag + 4;
+constexpr int kSmemUsed = kOffAbort + 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for the 1024-byte alignment
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
@@ -543,96 +542,6 @@ __device__ __forceinline__ void store_block(T* rows, int h0, int hvalid, int dim
     __syncwarp();
 }
 
-// ------------------------------------------------------------------------------------
-// fused combine
-// ------------------------------------------------------------------------------------
-// Called by all softmax threads once this CTA's piece of split unit s.unit (f16 O/l and
-// lse) is written. Each thread's stores are made visible device-wide, then one thread
-// takes a ticket on the unit's counter; the CTA whose ticket is the last of the unit's
-// pieces merges them: out = v_scale * sum_k 2^(lse_k - L) O_k / sum_k 2^(lse_k - L),
-// L = max_k lse_k (0 when every piece is empty). No thread waits on another CTA. The
-// other pieces are read through L2 (ld.global.cg), since this SM's L1 may hold lines of
-// the same slots from an earlier call.
-__device__ void arrive_and_merge(const DecodeParams& p, const Segment& s, int st, volatile int* flag_s) {
-    __threadfence();
-    named_bar_sync<kBarSoftmax, kSoftmaxThreads>();
-    const int64_t W = p.part.width;
-    const int64_t c_lo = cta_of_slot(p.part, static_cast<int64_t>(s.unit) * W);
-    const int64_t c_hi = cta_of_slot(p.part, (static_cast<int64_t>(s.unit) + 1) * W - 1);
-    if (st == 0) {
-        int n = 0;
-        for (int64_t c = c_lo; c <= c_hi; ++c) n += cta_begin(p.part, c) < cta_begin(p.part, c + 1) ? 1 : 0;
-        const int old = atomicAdd(p.arrivals + s.unit, 1);
-        __threadfence();
-        *flag_s = old == n - 1 ? 1 : 0;
-    }
-    named_bar_sync<kBarSoftmax, kSoftmaxThreads>();
-    if (!*flag_s) return;
-    // Thread st: head hl = st / 4, dims dq .. dq + 127 in four passes of 32.
-    const int hl = st >> 2, dq = (st & 3) * 128;
-    const int32_t h = s.group * kHeadsPerCta + hl;
-    // The host fuses only when a unit meets at most kFusedMaxPieces CTA ranges, so piece k
-    // is CTA c_lo + k (none when past c_hi or when that CTA's range is empty).
-    int32_t slot[kFusedMaxPieces];
-    float w[kFusedMaxPieces];
-    float m = kNegInf;
-#pragma unroll
-    for (int k = 0; k < kFusedMaxPieces; ++k) {
-        const int64_t c = c_lo + k;
-        const int64_t b = cta_begin(p.part, c);
-        const bool valid = c <= c_hi && b < cta_begin(p.part, c + 1);
-        slot[k] = valid ? static_cast<int32_t>(2 * c + (s.unit == b / W ? 0 : 1)) : 0;
-        w[k] = valid ? __ldcg(p.part_lse + static_cast<int64_t>(slot[k]) * kHeadsPerCta + hl) : kNegInf;
-        m = fmaxf(m, w[k]);
-    }
-    float wsum = 0.0f;
-#pragma unroll
-    for (int k = 0; k < kFusedMaxPieces; ++k) {
-        w[k] = (m != kNegInf && w[k] != kNegInf) ? ex2_approx(w[k] - m) : 0.0f;  // 0: no or empty piece
-        wsum += w[k];
-    }
-    const float f = wsum > 0.0f ? p.v_scale / wsum : 0.0f;
-    if (h >= p.heads) return;
-    __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) +
-                          (static_cast<int64_t>(s.row) * p.heads + h) * kLatent + dq;
-#pragma unroll 1
-    for (int pass = 0; pass < 4; ++pass) {
-        float acc[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) acc[e] = 0.0f;
-#pragma unroll
-        for (int k = 0; k < kFusedMaxPieces; ++k) {
-            if (w[k] != 0.0f) {
-                const uint4* src = reinterpret_cast<const uint4*>(
-                    p.part_o + (static_cast<int64_t>(slot[k]) * kHeadsPerCta + hl) * kLatent + dq + pass * 32);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint4 raw = __ldcg(src + q);
-                    const __half2* hv = reinterpret_cast<const __half2*>(&raw);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 v = __half22float2(hv[e]);
-                        acc[8 * q + 2 * e] += w[k] * v.x;
-                        acc[8 * q + 2 * e + 1] += w[k] * v.y;
-                    }
-                }
-            }
-        }
-        uint4* dst = reinterpret_cast<uint4*>(orow + pass * 32);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            uint4 packed;
-            uint32_t* pw = reinterpret_cast<uint32_t*>(&packed);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[8 * q + 2 * e] * f, acc[8 * q + 2 * e + 1] * f);
-                pw[e] = *reinterpret_cast<uint32_t*>(&b2);
-            }
-            dst[q] = packed;
-        }
-    }
-}
-
 __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase, uint32_t tmem,
                             volatile int* abort_flag, int nseg, const Segment& seg0) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -646,7 +555,6 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
     float* alpha_s = reinterpret_cast<float*>(smem + kOffAlpha);
     float* l_s = reinterpret_cast<float*>(smem + kOffL);
     float* f_s = reinterpret_cast<float*>(smem + kOffF);
-    volatile int* merge_flag_s = reinterpret_cast<volatile int*>(smem + kOffMergeFlag);
     static_assert(kSoftmaxWarps * 2048 <= 4 * kPTermBytes, "epilogue staging fits the P buffers");
     uint8_t* stage = smem + kOffP + sw * 2048;  // epilogue staging (2 KB per warp)
     auto barp = [&](int b) { return sbase + kOffBars + 8 * b; };
@@ -696,7 +604,6 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
                 uint4* po = reinterpret_cast<uint4*>(p.part_o + static_cast<int64_t>(s.part) * kHeadsPerCta * kLatent);
                 for (int e = st; e < kHeadsPerCta * kLatent / 8; e += kSoftmaxThreads) po[e] = make_uint4(0, 0, 0, 0);
                 if (st < kHeadsPerCta) p.part_lse[s.part * kHeadsPerCta + st] = kNegInf;
-                if (p.fused_combine) arrive_and_merge(p, s, st, merge_flag_s);
             }
             continue;
         }
@@ -893,7 +800,6 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(barp(BAR_OEMPTY));
-        if (!whole && p.fused_combine) arrive_and_merge(p, s, st, merge_flag_s);
         if (st == 0 && i == 0) DSA_TRACE_AT(p, 18);
         // The staging area is the P buffer and l_s / f_s are reused: the next unit starts
         // only after every softmax warp is done here.

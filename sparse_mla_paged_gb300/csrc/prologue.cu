@@ -152,8 +152,6 @@ __device__ void resolve_row(const PrologueParams& p, int32_t r, uint32_t* sm, in
     if (ids)
         for (int32_t j = tid; j < W; j += kResolveThreads) ids[j] = j < total ? ids_s[j] : -1;
     if (tid == 0) p.cnt[r] = total;
-    if (p.arrivals)
-        for (int32_t g = tid; g < p.groups; g += kResolveThreads) p.arrivals[static_cast<int64_t>(r) * p.groups + g] = 0;
     if (!offs) return;
     for (int32_t j0 = tid; j0 < total; j0 += kBatch * kResolveThreads) {
         // Cache byte offset of each id through the block table (decode_k.rs: physical =

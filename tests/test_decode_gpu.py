@@ -134,16 +134,6 @@ def test_more_ctas_than_slots(api, width, ctas):
     assert api.read_device_status(ws) == 0
 
 
-def test_fused_merge_beside_empty_ranges(api):
-    """Two rows of 3 slots over 8 CTAs: CTAs 0 and 4 have empty ranges, each row is split
-    over 3 CTAs and merged inside the decode kernel by the last of them to finish."""
-    w = wl.random_case(num_seqs=2, heads=64, seq_len=300, sel_width=3, hole_frac=0.0, dup_frac=0.0, seed=3)
-    ws = api.alloc_workspace(2, 1, 64, 3, num_ctas=8)
-    for _ in range(2):                                 # the piece counters start from zero every call
-        _check(api, w, "fused merge, 8 CTAs over 6 slots", workspace=ws, num_ctas=8, status_ok=False)
-        assert api.read_device_status(ws) == 0
-
-
 def test_empty_and_single_token_rows(api):
     w = wl.random_case(num_seqs=4, heads=64, seq_len=700, sel_width=300, hole_frac=0.0, dup_frac=0.0, seed=5)
     sel = w.sel_indices.clone()
