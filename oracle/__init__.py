@@ -11,6 +11,10 @@ source pages it restates:
 
 * ``attend.rs`` = spark_model/layers/glm5next_dsa/attend.rs
 * ``decode_k.rs`` = metrale_model_arch/glm5next_dsa/layer/decode_k.rs
+
+The cache writer (``latent_write``, ``e4m3_encode``) restates the ``latent_write`` launch
+of decode_k.rs ``decode_k``; its kernel body is not on the pages and the reading taken is
+written beside ``oracle_latent_write`` in ``dsa_oracle.c``.
 """
 from __future__ import annotations
 
@@ -60,6 +64,10 @@ def _bind(path: str):
     lib.oracle_dsa_mla_decode.restype = i32
     lib.oracle_online_cores.argtypes = []
     lib.oracle_online_cores.restype = i32
+    lib.oracle_e4m3_encode.argtypes = [f64]
+    lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+    lib.oracle_latent_write.argtypes = [P, P, P, i32, f64, f64, i32, i64, P, i64, P]
+    lib.oracle_latent_write.restype = i32
     return lib
 
 
@@ -164,3 +172,35 @@ def decode_workload(w, rows=None, threads: int = 0, lib=None) -> np.ndarray:
                   w.max_blocks_per_seq, h["seq_lens"], h["sel_indices"], w.num_seqs,
                   w.rows_per_seq, w.num_q_heads, w.block_size, w.cache_stride_bytes,
                   w.k_scale, w.v_scale, w.sm_scale, rows=rows, threads=threads, lib=lib)
+
+
+def e4m3_encode(values, lib=None) -> np.ndarray:
+    """E4M3 ("fn") codes of float64 values: round to nearest even, saturating to +-448."""
+    lib = lib or _load()
+    flat = np.ascontiguousarray(values, dtype=np.float64).ravel()
+    return np.array([lib.oracle_e4m3_encode(float(v)) for v in flat], dtype=np.uint8).reshape(np.shape(values))
+
+
+def latent_write(kv_a_bits, weight_bits, slots, rms_eps, kv_scale, block_size, cache_stride_bytes, cache,
+                 lib=None):
+    """decode_k.rs ``decode_k``, the ``latent_write`` launch: RMSNorm(kv_a) * w * (1/kv_scale)
+    stored as E4M3 at each row's slot (negative slot: skipped). ``cache`` (uint8, flat view
+    of the pool) is written in place. 1/kv_scale is formed in single precision, as the
+    launcher does. Returns the float64 values before rounding, [rows, 512]."""
+    x = np.ascontiguousarray(kv_a_bits, dtype=np.uint16).reshape(-1, LATENT)
+    w = np.ascontiguousarray(weight_bits, dtype=np.uint16).reshape(LATENT)
+    sl = np.ascontiguousarray(slots, dtype=np.int64).reshape(-1)
+    if sl.size != x.shape[0]:
+        raise ValueError("one slot per row")
+    if not (cache.flags["C_CONTIGUOUS"] and cache.dtype == np.uint8):
+        raise ValueError("cache must be a contiguous uint8 array")
+    inv = float(np.float32(1.0) / np.float32(kv_scale))
+    vals = np.zeros((x.shape[0], LATENT), dtype=np.float64)
+    rc = (lib or _load()).oracle_latent_write(_ptr(x), _ptr(w), _ptr(sl), x.shape[0], float(rms_eps), inv,
+                                              int(block_size), int(cache_stride_bytes), _ptr(cache),
+                                              cache.size, _ptr(vals))
+    if rc == -2:
+        raise ValueError("a slot falls outside the cache")
+    if rc != 0:
+        raise ValueError("oracle_latent_write: bad arguments")
+    return vals

@@ -283,3 +283,70 @@ int32_t oracle_dsa_mla_decode(const uint16_t* q, const uint8_t* k_cache, const u
 }
 
 int32_t oracle_online_cores(void) { return (int32_t)sysconf(_SC_NPROCESSORS_ONLN); }
+
+/* ------------------------------------------------------------------------------------
+ * Cache writer.
+ *
+ * [decode_k.rs] decode_k, the latent_write launch: for each new token the kernel is given
+ * the row's kv_a (kv_lora_rank BF16 values), the kv_a RMSNorm weight (BF16), the cache
+ * pool, the token's slot = physical*block_size + pos % block_size, rms_eps and
+ * 1/kv_scale (a single-precision value computed on the host). The kernel body is not on
+ * the pages. Reading taken: the plain RMSNorm followed by the cache scale,
+ *   y[c] = x[c] / sqrt(mean_c x^2 + eps) * w[c] * (1/kv_scale),
+ * stored as E4M3 (round to nearest even, saturating to +-448) at byte
+ *   (slot / block_size)*cache_stride_bytes + (slot % block_size)*512 + c,
+ * the layout the decode reads. A negative slot writes nothing.
+ * ---------------------------------------------------------------------------------- */
+
+/* E4M3 ("fn") code of v from the format's definition: magnitudes of 448 and above
+ * saturate to 448 (0x7E); normal values have 3 mantissa bits after the implicit 1 and
+ * exponents -6..8; below 2^-6 the subnormals m/8 * 2^-6. Ties round to the even code. */
+uint8_t oracle_e4m3_encode(double v) {
+    if (isnan(v)) return 0x7F;
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs(v);
+    if (a >= 448.0) return sign | 0x7E;
+    if (a < ldexp(1.0, -6)) {
+        double m = nearbyint(ldexp(a, 9)); /* units of 2^-9, round half to even */
+        if (m >= 8.0) return sign | 0x08;  /* rounded up to the smallest normal, 2^-6 */
+        return sign | (uint8_t)m;
+    }
+    int k;
+    double f = frexp(a, &k);                  /* a = f * 2^k, f in [0.5, 1) */
+    int e = k - 1;                            /* a = (2f) * 2^e, 2f in [1, 2) */
+    double m = nearbyint((2.0 * f - 1.0) * 8.0);
+    if (m >= 8.0) {
+        m = 0.0;
+        e += 1;
+    }
+    return sign | (uint8_t)((e + 7) << 3) | (uint8_t)m;
+}
+
+/* Writes rows tokens; values_out (may be NULL) receives each element's value before the
+ * E4M3 rounding, [rows, 512]. Returns 0, -1 on bad arguments, -2 when a slot's bytes fall
+ * outside cache_bytes. */
+int32_t oracle_latent_write(const uint16_t* kv_a, const uint16_t* weight, const int64_t* slots, int32_t rows,
+                            double rms_eps, double inv_kv_scale, int32_t block_size,
+                            int64_t cache_stride_bytes, uint8_t* cache, int64_t cache_bytes,
+                            double* values_out) {
+    if (rows < 0 || block_size < 1 || cache_stride_bytes < (int64_t)block_size * LATENT) return -1;
+    for (int32_t r = 0; r < rows; ++r) {
+        const int64_t slot = slots[r];
+        if (slot < 0) continue;
+        const uint16_t* x = kv_a + (int64_t)r * LATENT;
+        double sumsq = 0.0;
+        for (int c = 0; c < LATENT; ++c) {
+            double xc = oracle_bf16_to_f64(x[c]);
+            sumsq += xc * xc;
+        }
+        const double inv_rms = 1.0 / sqrt(sumsq / LATENT + rms_eps);
+        const int64_t base = (slot / block_size) * cache_stride_bytes + (slot % block_size) * LATENT;
+        if (base < 0 || base + LATENT > cache_bytes) return -2;
+        for (int c = 0; c < LATENT; ++c) {
+            double y = oracle_bf16_to_f64(x[c]) * inv_rms * oracle_bf16_to_f64(weight[c]) * inv_kv_scale;
+            if (values_out) values_out[(int64_t)r * LATENT + c] = y;
+            cache[base + c] = oracle_e4m3_encode(y);
+        }
+    }
+    return 0;
+}
