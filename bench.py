@@ -41,7 +41,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # ncu (dram__bytes_read.sum + dram__bytes_write.sum) on the decode kernel as it is now. A
 # workload absent here reports traffic null; an entry is dropped whenever the decode
 # kernel changes, until it is counted again.
-MEASURED_TRAFFIC = {}
+MEASURED_TRAFFIC = {"pooled_128k": 155117568, "ragged": 72865792, "verify_k4": 68007936, "decode_batch": 8966912}
 
 
 # ----------------------------------------------------------------------------------------
@@ -502,6 +502,62 @@ def run_reference(args, ws_n, rank):
 
 
 # ----------------------------------------------------------------------------------------
+# component: the cache writer
+# ----------------------------------------------------------------------------------------
+
+def run_latent_write(args):
+    """Times dsa_latent_write (RMSNorm + cache scale + E4M3 into scattered slots of a 1 GiB
+    pool) for `--rows` new tokens per call, 8 rotating input sets, in CUDA graphs. Bytes
+    per row: 1 KiB of kv_a read, 512 B written, the slot; the 1 KiB weight once per call."""
+    import sparse_mla_paged_gb300.api as api
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    rows, bs, pages = args.rows, 64, (1 << 30) // (64 * 512)
+    g = torch.Generator(device=device)
+    g.manual_seed(wl.BASE_SEED)
+    cache = torch.zeros(pages * bs * 512, dtype=torch.uint8, device=device)
+    sets = []
+    for _ in range(8):
+        x = torch.randn((rows, 512), generator=g, device=device).to(torch.bfloat16)
+        slots = torch.randperm(pages * bs, generator=g, device=device)[:rows].to(torch.int64)
+        sets.append((x, slots))
+    w = (0.5 + torch.rand(512, generator=g, device=device)).to(torch.bfloat16)
+    stream = torch.cuda.Stream(device)
+
+    def call(i):
+        x, sl = sets[i % 8]
+        api.latent_write(x, w, sl, 1e-6, 0.05, bs, bs * 512, cache, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            call(i)
+    stream.synchronize()
+    n = min(args.steps, 256)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(n):
+                call(i)
+        graph.replay()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = max(1, args.steps // n)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        e1.record(stream)
+    stream.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (reps * n)
+    nbytes = rows * (1024 + 512 + 8) + 1024
+    peaks, src = load_peaks()
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"component": "latent_write", "rows": rows, "value": round(us, 3), "unit": "us/call",
+            "bytes_per_call": nbytes, "calls": reps * n,
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": float(peaks["hbm_gbs"]),
+                         "unit": "GB/s", "frac": round(gbs / float(peaks["hbm_gbs"]), 4)}}
+
 
 def main():
     ap = argparse.ArgumentParser()
@@ -524,6 +580,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--component", choices=["latent_write"], default=None,
+                    help="time one component of the path instead of the decode step (its own JSON line)")
+    ap.add_argument("--rows", type=int, default=128, help="rows per call for --component latent_write")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per decode-kernel launch from an ncu capture of the current kernel")
     args = ap.parse_args()
@@ -538,6 +597,9 @@ def main():
     if not torch.cuda.is_available():
         print(json.dumps({"metric": METRIC, "error": "no CUDA device"}))
         return 1
+    if args.component == "latent_write":
+        print(json.dumps(run_latent_write(args)))
+        return 0
     init_dist(ws_n, "nccl")
     line = run_cuda(args, ws_n, rank, local)
     w0 = line.pop("_w0")

@@ -220,6 +220,28 @@ int32_t dsa_resolve_indices(const int32_t* sel_indices, const int32_t* seq_lens,
                             int32_t* counts_out, void* stream);
 
 /*
+ * dsa_latent_write: the cache writer that produces the rows the decode reads (decode_k.rs,
+ * decode_k: the latent_write launch, one per new token). For each row i with slots[i] >= 0:
+ *   y[c] = kv_a[i,c] / sqrt(mean_c kv_a[i,c]^2 + rms_eps) * norm_weight[c] * (1/kv_scale)
+ * is stored as E4M3 (round to nearest even, saturating to +-448) in the 512 bytes at
+ *   cache + (slots[i] / block_size)*cache_stride_bytes + (slots[i] % block_size)*512,
+ * slot = physical_page*block_size + position % block_size as the pages compute it. The
+ * kernel body is not on the pages; this RMSNorm-then-scale order is the plain reading.
+ * 1/kv_scale is formed in single precision, as the pages' launcher does.
+ *  kv_a         bf16 [rows, 512], 8-byte aligned (the kv_a projection of the new tokens).
+ *  norm_weight  bf16 [512], 8-byte aligned (the kv_a RMSNorm weight).
+ *  slots        int64 [rows], 8-byte aligned; a negative slot writes nothing.
+ *  rows >= 0; rms_eps >= 0; kv_scale finite and non-zero.
+ *  block_size, cache_stride_bytes  as for dsa_mla_decode (stride >= block_size*512, a
+ *               multiple of 16); cache 16-byte aligned.
+ * The pool size is not an argument: a slot past the pool is the caller's error, as a
+ * block-table entry past it is for the decode. Rows with the same slot race.
+ */
+int32_t dsa_latent_write(const void* kv_a, const void* norm_weight, const int64_t* slots,
+                         int32_t rows, float rms_eps, float kv_scale, int32_t block_size,
+                         int64_t cache_stride_bytes, void* cache, void* stream);
+
+/*
  * dsa_mla_decode_static: dsa_mla_decode for callers that cannot allocate device memory at
  * call time (for instance code running under a framework that owns all device memory
  * through its own pool, or a latency-critical path that cannot accept cudaMalloc's

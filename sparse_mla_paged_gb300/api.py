@@ -156,6 +156,23 @@ def resolve_indices(sel_indices: torch.Tensor, seq_lens: torch.Tensor, stream=No
     return ids, counts
 
 
+def latent_write(kv_a: torch.Tensor, norm_weight: torch.Tensor, slots: torch.Tensor, rms_eps: float,
+                 kv_scale: float, block_size: int, cache_stride_bytes: int, cache: torch.Tensor,
+                 stream=None) -> torch.Tensor:
+    """dsa_latent_write: RMSNorm(kv_a) * weight * (1/kv_scale) as E4M3 into each row's slot of
+    the paged cache (negative slot: skipped). Returns cache."""
+    _need(kv_a, torch.bfloat16, "kv_a")
+    _need(norm_weight, torch.bfloat16, "norm_weight")
+    _need(slots, torch.int64, "slots")
+    _need(cache, torch.uint8, "cache")
+    if kv_a.shape[-1] != LATENT or norm_weight.numel() != LATENT or slots.numel() != kv_a.numel() // LATENT:
+        raise ValueError("kv_a [rows, 512], norm_weight [512], slots [rows]")
+    check(_lib.load().dsa_latent_write(_ptr(kv_a), _ptr(norm_weight), _ptr(slots), int(slots.numel()),
+                                       float(rms_eps), float(kv_scale), int(block_size), int(cache_stride_bytes),
+                                       _ptr(cache), _stream(stream)), "dsa_latent_write")
+    return cache
+
+
 def read_device_status(workspace: torch.Tensor, stream=None) -> int:
     v = _lib.ctypes.c_int32(0)
     check(_lib.load().dsa_read_device_status(_ptr(workspace), _lib.ctypes.byref(v), _stream(stream)),

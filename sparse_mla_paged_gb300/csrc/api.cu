@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -529,6 +530,33 @@ int32_t dsa_resolve_indices(const int32_t* sel_indices, const int32_t* seq_lens,
     pp.groups = 1;
     pp.rows_per_seq = 1;
     return from_cuda(launch_prologue(pp, rows, false, static_cast<cudaStream_t>(stream)));
+}
+
+int32_t dsa_latent_write(const void* kv_a, const void* norm_weight, const int64_t* slots, int32_t rows,
+                         float rms_eps, float kv_scale, int32_t block_size, int64_t cache_stride_bytes, void* cache,
+                         void* stream) {
+    if (!kv_a || !norm_weight || !slots || !cache || rows < 0 || block_size < 1) return DSA_ERR_INVALID_ARGUMENT;
+    if (!aligned(kv_a, 8) || !aligned(norm_weight, 8) || !aligned(slots, 8) || !aligned(cache, 16))
+        return DSA_ERR_INVALID_ARGUMENT;
+    if (cache_stride_bytes < static_cast<int64_t>(block_size) * kLatent || cache_stride_bytes % 16 != 0)
+        return DSA_ERR_INVALID_ARGUMENT;
+    if (!(rms_eps >= 0.0f) || !std::isfinite(rms_eps) || !std::isfinite(kv_scale) || kv_scale == 0.0f)
+        return DSA_ERR_INVALID_ARGUMENT;
+    if (rows == 0) return DSA_OK;
+    DeviceState* d = nullptr;
+    int32_t st = current_device(&d);
+    if (st != DSA_OK) return st;
+    LatentWriteParams p{};
+    p.kv_a = static_cast<const uint16_t*>(kv_a);
+    p.weight = static_cast<const uint16_t*>(norm_weight);
+    p.slots = reinterpret_cast<const long long*>(slots);
+    p.cache = static_cast<uint8_t*>(cache);
+    p.cache_stride = cache_stride_bytes;
+    p.rows = rows;
+    p.block_size = block_size;
+    p.eps = rms_eps;
+    p.inv_scale = 1.0f / kv_scale;  // formed in single precision, as the pages' launcher does
+    return from_cuda(launch_latent_write(p, static_cast<cudaStream_t>(stream)));
 }
 
 int32_t dsa_read_device_status(const void* workspace, int32_t* status_out, void* stream) {

@@ -192,6 +192,17 @@ struct CombineParams {
     int32_t early_dependents;  // let the next kernel launch as soon as every block has started
 };
 
+struct LatentWriteParams {
+    const uint16_t* kv_a;      // bf16 bits [rows, 512]
+    const uint16_t* weight;    // bf16 bits [512]: the kv_a RMSNorm weight
+    const long long* slots;    // [rows]; a negative slot writes nothing
+    uint8_t* cache;            // E4M3 pool
+    int64_t cache_stride;      // bytes per page
+    int32_t rows, block_size;
+    float eps;                 // rms_eps
+    float inv_scale;           // 1/kv_scale
+};
+
 // Launchers (each defined next to its kernel).
 // The decode and combine kernels are launched as programmatic dependents of the kernel
 // before them on the stream (they start their set-up early and wait on the grid
@@ -210,6 +221,7 @@ cudaError_t launch_decode_128(const DecodeParams& p, const CUtensorMap& kmap, co
                               cudaStream_t stream);
 // max_pieces: the most CTAs sharing one unit (max_pieces_per_unit; selects the variant).
 cudaError_t launch_combine(const CombineParams& p, int units, int max_pieces, cudaStream_t stream);
+cudaError_t launch_latent_write(const LatentWriteParams& p, cudaStream_t stream);
 cudaError_t decode_kernel_setup_64();
 cudaError_t decode_kernel_setup_128();
 cudaError_t prologue_kernel_setup();

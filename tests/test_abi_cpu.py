@@ -120,3 +120,18 @@ def test_workspace_size_grows_with_the_problem(lib):
     assert base >= rows * width * (4 + 8) + rows * 4 + rows * 65536 + 2 * ctas * 64 * 512 * 2
     assert f(0, 1, 64, 2048, 152) == 0
 
+
+
+def test_latent_write_rejects_bad_arguments_on_host(lib):
+    f = lib.dsa_latent_write
+    ok = dict(x=0x10000, w=0x20000, s=0x30000, rows=4, eps=1e-6, ks=0.05, bs=64, stride=64 * 512, c=0x40000)
+
+    def call(**over):
+        a = dict(ok, **over)
+        return f(a["x"], a["w"], a["s"], a["rows"], a["eps"], a["ks"], a["bs"], a["stride"], a["c"], None)
+
+    for over in (dict(x=0), dict(w=0), dict(s=0), dict(c=0), dict(rows=-1), dict(bs=0), dict(ks=0.0),
+                 dict(eps=-1.0), dict(stride=64 * 512 - 16), dict(stride=64 * 512 + 8), dict(x=0x10004),
+                 dict(s=0x30004), dict(c=0x40008)):
+        assert call(**over) == 1, over
+    assert call(rows=0) == 0                        # nothing to write: no device needed
