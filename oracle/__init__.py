@@ -68,6 +68,8 @@ def _bind(path: str):
     lib.oracle_e4m3_encode.restype = ctypes.c_uint8
     lib.oracle_latent_write.argtypes = [P, P, P, i32, f64, f64, i32, i64, P, i64, P]
     lib.oracle_latent_write.restype = i32
+    lib.oracle_select_pools.argtypes = [P, P, i32, i32, i32, i32, P]
+    lib.oracle_select_pools.restype = i32
     return lib
 
 
@@ -204,3 +206,19 @@ def latent_write(kv_a_bits, weight_bits, slots, rms_eps, kv_scale, block_size, c
     if rc != 0:
         raise ValueError("oracle_latent_write: bad arguments")
     return vals
+
+
+def select_pools(scores, q_pos, kpool: int, topk: int, lib=None) -> np.ndarray:
+    """The selector the decode's input comes from (attend.rs module doc; decode_k.rs
+    decode_k): per row, the ``topk`` highest-scoring pools among those ending at or before
+    q_pos (equal scores: lower pool first; NaN lowest), listed in ascending position as
+    ``kpool`` consecutive token ids each, -1 padded to ``topk * kpool``. scores: float32
+    [rows, n_pools]; q_pos: int32 [rows]. Returns int32 [rows, topk * kpool]."""
+    sc = np.ascontiguousarray(scores, dtype=np.float32)
+    rows, n_pools = sc.shape
+    qp = np.ascontiguousarray(q_pos, dtype=np.int32).reshape(rows)
+    out = np.empty((rows, topk * kpool), dtype=np.int32)
+    rc = (lib or _load()).oracle_select_pools(_ptr(sc), _ptr(qp), rows, n_pools, int(kpool), int(topk), _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_select_pools: bad arguments")
+    return out

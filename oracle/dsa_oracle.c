@@ -350,3 +350,61 @@ int32_t oracle_latent_write(const uint16_t* kv_a, const uint16_t* weight, const 
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------------------
+ * Selector.
+ *
+ * [attend.rs] module doc: the decode consumes a [q_rows, out_width] i32 row of token ids
+ * with -1 holes, produced by the selector; [attend.rs] DsaDecodePaging::validate: pools
+ * are built over absolute positions, index_kpool positions each; [decode_k.rs] decode_k:
+ * the selection takes index_topk pools, and row r only takes pools that end at or before
+ * its position q_pos[r]. The selector's body is not on the pages. Reading taken: pool p
+ * (positions p*kpool .. p*kpool + kpool - 1) is eligible for row r when
+ * (p + 1)*kpool - 1 <= q_pos[r]; the index_topk eligible pools of highest score are taken
+ * (equal scores: the lower pool first; NaN ranks below every number); the row lists the
+ * taken pools in ascending position, each as its kpool consecutive ids, then -1 up to
+ * index_topk*kpool entries.
+ * ---------------------------------------------------------------------------------- */
+
+typedef struct {
+    float score;
+    int32_t pool;
+} pool_rank_t;
+
+/* Orders by score descending (NaN last), then pool ascending. */
+static int cmp_pool_rank(const void* a, const void* b) {
+    const pool_rank_t* x = (const pool_rank_t*)a;
+    const pool_rank_t* y = (const pool_rank_t*)b;
+    int xn = isnan(x->score), yn = isnan(y->score);
+    if (xn != yn) return xn - yn;
+    if (!xn && x->score != y->score) return x->score > y->score ? -1 : 1;
+    return (x->pool > y->pool) - (x->pool < y->pool);
+}
+
+int32_t oracle_select_pools(const float* scores, const int32_t* q_pos, int32_t rows, int32_t n_pools,
+                            int32_t kpool, int32_t topk, int32_t* ids_out) {
+    if (rows < 0 || n_pools < 0 || kpool < 1 || topk < 1) return -1;
+    pool_rank_t* cand = (pool_rank_t*)malloc(sizeof(pool_rank_t) * (size_t)(n_pools > 0 ? n_pools : 1));
+    int32_t* taken = (int32_t*)malloc(sizeof(int32_t) * (size_t)topk);
+    for (int32_t r = 0; r < rows; ++r) {
+        int32_t n = 0;
+        for (int32_t p = 0; p < n_pools; ++p)
+            if ((int64_t)(p + 1) * kpool - 1 <= (int64_t)q_pos[r]) {
+                cand[n].score = scores[(int64_t)r * n_pools + p];
+                cand[n].pool = p;
+                ++n;
+            }
+        qsort(cand, (size_t)n, sizeof(pool_rank_t), cmp_pool_rank);
+        int32_t m = n < topk ? n : topk;
+        for (int32_t i = 0; i < m; ++i) taken[i] = cand[i].pool;
+        qsort(taken, (size_t)m, sizeof(int32_t), cmp_i32);
+        int32_t* out = ids_out + (int64_t)r * topk * kpool;
+        int64_t o = 0;
+        for (int32_t i = 0; i < m; ++i)
+            for (int32_t t = 0; t < kpool; ++t) out[o++] = taken[i] * kpool + t;
+        for (; o < (int64_t)topk * kpool; ++o) out[o] = -1;
+    }
+    free(cand);
+    free(taken);
+    return 0;
+}
