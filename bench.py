@@ -505,6 +505,39 @@ def run_reference(args, ws_n, rank):
 # component: the cache writer
 # ----------------------------------------------------------------------------------------
 
+def _time_in_graphs(call, steps, warmup, stream) -> tuple[float, int]:
+    """Average device time of call(i) in microseconds: up to 256 calls captured in one CUDA
+    graph, the graph replayed until `steps` calls ran; CUDA events on the launching stream."""
+    with torch.cuda.stream(stream):
+        for i in range(max(warmup, 3)):
+            call(i)
+    stream.synchronize()
+    n = min(steps, 256)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(n):
+                call(i)
+        graph.replay()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = max(1, steps // n)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        e1.record(stream)
+    stream.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (reps * n), reps * n
+
+
+def _hbm_roofline(nbytes: int, us: float) -> dict:
+    peaks, _ = load_peaks()
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"bound": "hbm", "achieved": round(gbs, 1), "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+            "frac": round(gbs / float(peaks["hbm_gbs"]), 4)}
+
+
 def run_latent_write(args):
     """Times dsa_latent_write (RMSNorm + cache scale + E4M3 into scattered slots of a 1 GiB
     pool) for `--rows` new tokens per call, 8 rotating input sets, in CUDA graphs. Bytes
@@ -529,34 +562,34 @@ def run_latent_write(args):
         x, sl = sets[i % 8]
         api.latent_write(x, w, sl, 1e-6, 0.05, bs, bs * 512, cache, stream=stream)
 
-    with torch.cuda.stream(stream):
-        for i in range(max(args.warmup, 3)):
-            call(i)
-    stream.synchronize()
-    n = min(args.steps, 256)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        with torch.cuda.graph(graph, stream=stream):
-            for i in range(n):
-                call(i)
-        graph.replay()
-    stream.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    reps = max(1, args.steps // n)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(reps):
-            graph.replay()
-        e1.record(stream)
-    stream.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / (reps * n)
+    us, calls = _time_in_graphs(call, args.steps, args.warmup, stream)
     nbytes = rows * (1024 + 512 + 8) + 1024
-    peaks, src = load_peaks()
-    gbs = nbytes / (us * 1e-6) / 1e9
     return {"component": "latent_write", "rows": rows, "value": round(us, 3), "unit": "us/call",
-            "bytes_per_call": nbytes, "calls": reps * n,
-            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": float(peaks["hbm_gbs"]),
-                         "unit": "GB/s", "frac": round(gbs / float(peaks["hbm_gbs"]), 4)}}
+            "bytes_per_call": nbytes, "calls": calls, "roofline": _hbm_roofline(nbytes, us)}
+
+
+def run_select(args):
+    """Times dsa_select_pools on the pooled 128K shape: `--rows` rows (default 128) of 32768
+    pooled scores, 512 pools of 4 per row, every pool eligible; 16 rotating input sets
+    (268 MB, above L2). Bytes per call: the scores and positions read, the ids written."""
+    import sparse_mla_paged_gb300.api as api
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    rows, n_pools, kpool, topk = args.rows, 32768, 4, 512
+    sets = [wl.pool_scores(rows, n_pools, kpool, device=device, seed=wl.BASE_SEED + i) for i in range(16)]
+    outs = [torch.empty((rows, topk * kpool), dtype=torch.int32, device=device) for _ in range(2)]
+    stream = torch.cuda.Stream(device)
+
+    def call(i):
+        sc, q = sets[i % 16]
+        api.select_pools(sc, q, kpool, topk, out=outs[i % 2], stream=stream)
+
+    us, calls = _time_in_graphs(call, args.steps, args.warmup, stream)
+    nbytes = rows * (n_pools * 4 + 4 + topk * kpool * 4)
+    return {"component": "select", "rows": rows, "n_pools": n_pools, "kpool": kpool, "index_topk": topk,
+            "value": round(us, 3), "unit": "us/call", "bytes_per_call": nbytes, "calls": calls,
+            "roofline": _hbm_roofline(nbytes, us)}
 
 
 def main():
@@ -580,9 +613,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
-    ap.add_argument("--component", choices=["latent_write"], default=None,
+    ap.add_argument("--component", choices=["latent_write", "select"], default=None,
                     help="time one component of the path instead of the decode step (its own JSON line)")
-    ap.add_argument("--rows", type=int, default=128, help="rows per call for --component latent_write")
+    ap.add_argument("--rows", type=int, default=128, help="rows per call for --component latent_write / select")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per decode-kernel launch from an ncu capture of the current kernel")
     args = ap.parse_args()
@@ -597,8 +630,8 @@ def main():
     if not torch.cuda.is_available():
         print(json.dumps({"metric": METRIC, "error": "no CUDA device"}))
         return 1
-    if args.component == "latent_write":
-        print(json.dumps(run_latent_write(args)))
+    if args.component is not None:
+        print(json.dumps({"latent_write": run_latent_write, "select": run_select}[args.component](args)))
         return 0
     init_dist(ws_n, "nccl")
     line = run_cuda(args, ws_n, rank, local)

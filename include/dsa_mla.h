@@ -228,10 +228,11 @@ int32_t dsa_resolve_indices(const int32_t* sel_indices, const int32_t* seq_lens,
  * slot = physical_page*block_size + position % block_size as the pages compute it. The
  * kernel body is not on the pages; this RMSNorm-then-scale order is the plain reading.
  * 1/kv_scale is formed in single precision, as the pages' launcher does.
- *  kv_a         bf16 [rows, 512], 8-byte aligned (the kv_a projection of the new tokens).
- *  norm_weight  bf16 [512], 8-byte aligned (the kv_a RMSNorm weight).
+ *  kv_a         bf16 [rows, 512], 16-byte aligned (the kv_a projection of the new tokens).
+ *  norm_weight  bf16 [512], 16-byte aligned (the kv_a RMSNorm weight).
  *  slots        int64 [rows], 8-byte aligned; a negative slot writes nothing.
- *  rows >= 0; rms_eps >= 0; kv_scale finite and non-zero.
+ *  rows >= 0 (kv_a and slots may be null when rows == 0); rms_eps >= 0; kv_scale finite
+ *  and non-zero.
  *  block_size, cache_stride_bytes  as for dsa_mla_decode (stride >= block_size*512, a
  *               multiple of 16); cache 16-byte aligned.
  * The pool size is not an argument: a slot past the pool is the caller's error, as a
@@ -240,6 +241,25 @@ int32_t dsa_resolve_indices(const int32_t* sel_indices, const int32_t* seq_lens,
 int32_t dsa_latent_write(const void* kv_a, const void* norm_weight, const int64_t* slots,
                          int32_t rows, float rms_eps, float kv_scale, int32_t block_size,
                          int64_t cache_stride_bytes, void* cache, void* stream);
+
+/*
+ * dsa_select_pools: the selector that makes the decode's sel_indices rows (attend.rs
+ * module doc: a [q_rows, width] row of token ids with -1 holes; decode_k.rs decode_k: the
+ * index_topk pools of highest indexer score, row r taking only pools that end at or before
+ * its position q_pos[r]). Pool p covers positions p*kpool .. p*kpool + kpool - 1 and is
+ * eligible for row r when (p + 1)*kpool - 1 <= q_pos[r]. Per row, the topk eligible pools
+ * of highest score are taken (equal scores: the lower pool; NaN ranks below every number;
+ * -0 equals +0) and written in ascending position, kpool consecutive ids each, then -1 up
+ * to topk*kpool entries. The selector's body is not on the pages; this is the reading taken.
+ *  scores   float32 [rows, n_pools] pooled scores; q_pos int32 [rows]; ids_out int32
+ *           [rows, topk*kpool]; all 4-byte aligned.
+ *  rows, n_pools >= 0 (the arrays may be null when rows == 0, scores when n_pools == 0);
+ *  kpool, topk >= 1; n_pools*kpool and topk*kpool below 2^31
+ *  (DSA_ERR_UNSUPPORTED otherwise).
+ */
+int32_t dsa_select_pools(const float* scores, const int32_t* q_pos, int32_t rows,
+                         int32_t n_pools, int32_t kpool, int32_t topk, int32_t* ids_out,
+                         void* stream);
 
 /*
  * dsa_mla_decode_static: dsa_mla_decode for callers that cannot allocate device memory at

@@ -173,6 +173,21 @@ def latent_write(kv_a: torch.Tensor, norm_weight: torch.Tensor, slots: torch.Ten
     return cache
 
 
+def select_pools(scores: torch.Tensor, q_pos: torch.Tensor, kpool: int, topk: int, out=None,
+                 stream=None) -> torch.Tensor:
+    """dsa_select_pools: per row the topk highest-scoring pools ending at or before q_pos, as
+    ascending token ids (kpool per pool), -1 padded; returns int32 [rows, topk * kpool]."""
+    _need(scores, torch.float32, "scores")
+    _need(q_pos, torch.int32, "q_pos")
+    rows, n_pools = scores.shape
+    if out is None:
+        out = torch.empty((rows, topk * kpool), dtype=torch.int32, device=scores.device)
+    _need(out, torch.int32, "out")
+    check(_lib.load().dsa_select_pools(_ptr(scores), _ptr(q_pos), int(rows), int(n_pools), int(kpool), int(topk),
+                                       _ptr(out), _stream(stream)), "dsa_select_pools")
+    return out
+
+
 def read_device_status(workspace: torch.Tensor, stream=None) -> int:
     v = _lib.ctypes.c_int32(0)
     check(_lib.load().dsa_read_device_status(_ptr(workspace), _lib.ctypes.byref(v), _stream(stream)),

@@ -16,12 +16,12 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdsa_mla.so")
-SOURCES = ["api.cu", "prologue.cu", "decode.cu", "combine.cu", "static_scratch.cu", "latent_write.cu"]
+SOURCES = ["api.cu", "prologue.cu", "decode.cu", "combine.cu", "static_scratch.cu", "latent_write.cu", "select.cu"]
 # Translation units: (source, object, extra flags); decode.cu is built once per tile size.
 UNITS = [("api.cu", "api.o", []), ("prologue.cu", "prologue.o", []),
          ("decode.cu", "decode64.o", ["-DDSA_TILE=64"]), ("decode.cu", "decode128.o", ["-DDSA_TILE=128"]),
          ("combine.cu", "combine.o", []), ("static_scratch.cu", "static_scratch.o", []),
-         ("latent_write.cu", "latent_write.o", [])]
+         ("latent_write.cu", "latent_write.o", []), ("select.cu", "select.o", [])]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

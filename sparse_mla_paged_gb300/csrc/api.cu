@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <climits>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -98,6 +99,7 @@ int32_t current_device(DeviceState** out) {
             if (d.status == DSA_OK) d.status = from_cuda(decode_kernel_setup_128());
             if (d.status == DSA_OK) d.status = from_cuda(prologue_kernel_setup());
             if (d.status == DSA_OK) d.status = from_cuda(combine_kernel_setup());
+            if (d.status == DSA_OK) d.status = from_cuda(select_kernel_setup());
         }
         d.checked = true;
     }
@@ -535,8 +537,9 @@ int32_t dsa_resolve_indices(const int32_t* sel_indices, const int32_t* seq_lens,
 int32_t dsa_latent_write(const void* kv_a, const void* norm_weight, const int64_t* slots, int32_t rows,
                          float rms_eps, float kv_scale, int32_t block_size, int64_t cache_stride_bytes, void* cache,
                          void* stream) {
-    if (!kv_a || !norm_weight || !slots || !cache || rows < 0 || block_size < 1) return DSA_ERR_INVALID_ARGUMENT;
-    if (!aligned(kv_a, 8) || !aligned(norm_weight, 8) || !aligned(slots, 8) || !aligned(cache, 16))
+    if (!norm_weight || !cache || rows < 0 || block_size < 1) return DSA_ERR_INVALID_ARGUMENT;
+    if (rows > 0 && (!kv_a || !slots)) return DSA_ERR_INVALID_ARGUMENT;
+    if (!aligned(kv_a, 16) || !aligned(norm_weight, 16) || !aligned(slots, 8) || !aligned(cache, 16))
         return DSA_ERR_INVALID_ARGUMENT;
     if (cache_stride_bytes < static_cast<int64_t>(block_size) * kLatent || cache_stride_bytes % 16 != 0)
         return DSA_ERR_INVALID_ARGUMENT;
@@ -557,6 +560,28 @@ int32_t dsa_latent_write(const void* kv_a, const void* norm_weight, const int64_
     p.eps = rms_eps;
     p.inv_scale = 1.0f / kv_scale;  // formed in single precision, as the pages' launcher does
     return from_cuda(launch_latent_write(p, static_cast<cudaStream_t>(stream)));
+}
+
+int32_t dsa_select_pools(const float* scores, const int32_t* q_pos, int32_t rows, int32_t n_pools, int32_t kpool,
+                         int32_t topk, int32_t* ids_out, void* stream) {
+    if (rows < 0 || n_pools < 0 || kpool < 1 || topk < 1) return DSA_ERR_INVALID_ARGUMENT;
+    if (rows > 0 && (!q_pos || !ids_out || (n_pools > 0 && !scores))) return DSA_ERR_INVALID_ARGUMENT;
+    if (!aligned(scores, 4) || !aligned(q_pos, 4) || !aligned(ids_out, 4)) return DSA_ERR_INVALID_ARGUMENT;
+    if (static_cast<int64_t>(n_pools) * kpool > INT32_MAX || static_cast<int64_t>(topk) * kpool > INT32_MAX)
+        return DSA_ERR_UNSUPPORTED;
+    if (rows == 0) return DSA_OK;
+    DeviceState* d = nullptr;
+    int32_t st = current_device(&d);
+    if (st != DSA_OK) return st;
+    SelectParams p{};
+    p.scores = scores;
+    p.q_pos = q_pos;
+    p.ids = ids_out;
+    p.rows = rows;
+    p.n_pools = n_pools;
+    p.kpool = kpool;
+    p.topk = topk;
+    return from_cuda(launch_select(p, static_cast<cudaStream_t>(stream)));
 }
 
 int32_t dsa_read_device_status(const void* workspace, int32_t* status_out, void* stream) {

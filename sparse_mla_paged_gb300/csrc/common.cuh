@@ -203,6 +203,13 @@ struct LatentWriteParams {
     float inv_scale;           // 1/kv_scale
 };
 
+struct SelectParams {
+    const float* scores;       // [rows, n_pools] pooled indexer scores
+    const int32_t* q_pos;      // [rows] position of each query row
+    int32_t* ids;              // [rows, topk * kpool] token ids, -1 padded
+    int32_t rows, n_pools, kpool, topk;
+};
+
 // Launchers (each defined next to its kernel).
 // The decode and combine kernels are launched as programmatic dependents of the kernel
 // before them on the stream (they start their set-up early and wait on the grid
@@ -222,6 +229,8 @@ cudaError_t launch_decode_128(const DecodeParams& p, const CUtensorMap& kmap, co
 // max_pieces: the most CTAs sharing one unit (max_pieces_per_unit; selects the variant).
 cudaError_t launch_combine(const CombineParams& p, int units, int max_pieces, cudaStream_t stream);
 cudaError_t launch_latent_write(const LatentWriteParams& p, cudaStream_t stream);
+cudaError_t select_kernel_setup();
+cudaError_t launch_select(const SelectParams& p, cudaStream_t stream);
 cudaError_t decode_kernel_setup_64();
 cudaError_t decode_kernel_setup_128();
 cudaError_t prologue_kernel_setup();

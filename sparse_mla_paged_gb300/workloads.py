@@ -285,6 +285,21 @@ def verify_k4(device="cpu", seed: Optional[int] = None, num_seqs: Optional[int] 
 CONFIGS = [tiny, decode_batch, ragged, pooled_128k, verify_k4]
 
 
+def pool_scores(rows: int = 128, n_pools: int = 32768, kpool: int = 4, q_pos=None, device="cpu",
+                seed: Optional[int] = None) -> tuple[torch.Tensor, torch.Tensor]:
+    """Selector input of the pooled 128K decode: float32 pooled indexer scores [rows,
+    n_pools] ~ N(0, 1) (the indexer's weights are not on the pages, so its scores are
+    drawn) and each row's position q_pos (int32 [rows]; default: the last position,
+    n_pools*kpool - 1, so every pool is eligible). A list or tensor q_pos is taken as given."""
+    g = _gen(device, BASE_SEED + 7 if seed is None else seed)
+    scores = torch.randn((rows, n_pools), generator=g, device=device, dtype=torch.float32)
+    if q_pos is None:
+        q = torch.full((rows,), n_pools * kpool - 1, dtype=torch.int32, device=device)
+    else:
+        q = torch.as_tensor(q_pos, dtype=torch.int32).to(device)
+    return scores, q
+
+
 def config(index: int, device="cpu", seed: Optional[int] = None, num_seqs: Optional[int] = None) -> Workload:
     if num_seqs is None:
         return CONFIGS[index](device=device, seed=seed)

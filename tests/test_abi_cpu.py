@@ -26,7 +26,7 @@ def test_header_declares_expected_entry_points():
     names = _declared_functions()
     for want in ("dsa_mla_decode", "dsa_mla_decode_k", "dsa_mla_decode_ws", "dsa_resolve_indices",
                  "dsa_mla_decode_workspace_bytes", "dsa_status_string", "dsa_read_device_status",
-                 "dsa_mla_decode_host"):
+                 "dsa_mla_decode_host", "dsa_latent_write", "dsa_select_pools"):
         assert want in names
 
 
@@ -131,7 +131,24 @@ def test_latent_write_rejects_bad_arguments_on_host(lib):
         return f(a["x"], a["w"], a["s"], a["rows"], a["eps"], a["ks"], a["bs"], a["stride"], a["c"], None)
 
     for over in (dict(x=0), dict(w=0), dict(s=0), dict(c=0), dict(rows=-1), dict(bs=0), dict(ks=0.0),
-                 dict(eps=-1.0), dict(stride=64 * 512 - 16), dict(stride=64 * 512 + 8), dict(x=0x10004),
+                 dict(eps=-1.0), dict(stride=64 * 512 - 16), dict(stride=64 * 512 + 8), dict(x=0x10004), dict(x=0x10008), dict(w=0x20008),
                  dict(s=0x30004), dict(c=0x40008)):
         assert call(**over) == 1, over
     assert call(rows=0) == 0                        # nothing to write: no device needed
+    assert call(rows=0, x=0, s=0) == 0              # no rows: the row arrays may be null
+
+
+def test_select_rejects_bad_arguments_on_host(lib):
+    f = lib.dsa_select_pools
+    ok = dict(sc=0x10000, q=0x20000, rows=4, n=100, kpool=4, topk=8, ids=0x30000)
+
+    def call(**over):
+        a = dict(ok, **over)
+        return f(a["sc"], a["q"], a["rows"], a["n"], a["kpool"], a["topk"], a["ids"], None)
+
+    for over in (dict(sc=0), dict(q=0), dict(ids=0), dict(rows=-1), dict(n=-1), dict(kpool=0), dict(topk=0),
+                 dict(sc=0x10002), dict(q=0x20001), dict(ids=0x30002)):
+        assert call(**over) == 1, over
+    assert call(n=1 << 30, kpool=4) == 2            # token ids would pass 2^31
+    assert call(topk=1 << 29, kpool=8) == 2
+    assert call(rows=0, sc=0, q=0, ids=0) == 0       # nothing to select: no device needed
