@@ -12,13 +12,14 @@
 // and how many pools with key T are still to be taken.
 // * Rows of at most 40960 pools (select_staged_kernel): the keys are staged once in shared
 //   memory while the first digit's histogram is built. Thread t then owns pools 32t ..
-//   32t + 31 (per round of 32768 pools) and works on 32-bit masks of them: it lists the
-//   pools in T's first-digit bin (a few hundred for spread scores) as candidates, each warp
-//   in a region of its own; the other two digits are resolved on the candidates alone (on
-//   every key when a region overflows). A last pass marks the pools above T and equal to
-//   T; one block scan of both counts ranks the equal ones (the lowest-numbered are kept
-//   up to the count still needed) and gives each thread its output position, and the
-//   taken pools are written in ascending order.
+//   32t + 31 (per round of 32768 pools) and works on 32-bit masks of them: each warp lists
+//   its pools in T's first-digit bin (a few hundred in all for spread scores) in a region
+//   of its own, and counts the other two digits over that list (over its threads' own
+//   pools when the list overflowed). A last pass marks the pools above T and equal to T;
+//   one block scan of both counts ranks the equal ones (the lowest-numbered are kept up to
+//   the count still needed) and gives each thread its output position, and the taken pools
+//   are written in ascending order. Block barriers are the cost after staging, so block
+//   scans and histograms are double-buffered: nine barriers follow the staging.
 // * Longer rows (select_kernel): the three digit passes re-read the scores from global
 //   memory; each warp then owns a contiguous segment of pools, counts its keys above and
 //   equal to T, one scan over the warps gives every warp its output offset, and a second
@@ -47,10 +48,19 @@ constexpr int kCandidates = 4096;       // threshold-bin candidates kept in shar
 constexpr int kWarpCandidates = kCandidates / kSelectWarps;  // a private region per warp
 constexpr int kLoadBatch = 8;           // 16-byte score loads in flight per thread
 
+static_assert(kSelectWarps == 32, "a warp reads all warp totals, one per lane");
+
+// Warp totals for block scans, double-buffered: scan k writes buffer k % 2, so one barrier
+// per scan suffices (a buffer is written again only after the next scan's barrier, which
+// every reader of it has passed).
+struct ScanState {
+    uint32_t (*buf)[kSelectWarps];
+    int parity;
+};
+
 // Exclusive prefix sum over the block, in unsigned (wrapping) arithmetic; *total receives
-// the block total. Every thread of the block must call it (it has block barriers): a warp
-// scan, one warp scanning the warp totals, then each thread adds its warp's offset.
-__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* warp_sums, uint32_t* total) {
+// the block total. Every thread of the block must call it (one block barrier).
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, ScanState& st, uint32_t* total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint32_t x = v;
 #pragma unroll
@@ -58,30 +68,21 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* w
         const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
         if (lane >= o) x += y;
     }
-    if (lane == 31) warp_sums[warp] = x;
+    uint32_t* sums = st.buf[st.parity];
+    st.parity ^= 1;
+    if (lane == 31) sums[warp] = x;
     __syncthreads();
-    if (warp == 0) {
-        uint32_t w = lane < kSelectWarps ? warp_sums[lane] : 0u;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
-            if (lane >= o) w += y;
-        }
-        if (lane < kSelectWarps) warp_sums[lane] = w;  // inclusive
-    }
-    __syncthreads();
-    const uint32_t before = (warp > 0 ? warp_sums[warp - 1] : 0u) + x - v;
-    *total = warp_sums[kSelectWarps - 1];
-    __syncthreads();  // warp_sums may be reused by the next scan
-    return before;
+    const uint32_t t = sums[lane];
+    *total = __reduce_add_sync(0xffffffffu, t);
+    return __reduce_add_sync(0xffffffffu, lane < warp ? t : 0u) + x - v;
 }
 
 // Radix step shared by both kernels: given the digit histogram, the thread whose bins
 // (kBinsPerThread of them, counted from the top: thread 0 holds 2047 down) hold the
 // crossing point where the count from above reaches need records the digit and the count
-// still needed in it.
-__device__ __forceinline__ void find_crossing(const int32_t* hist, int32_t need, uint32_t* warp_sums,
-                                              uint32_t* sh_digit, int32_t* sh_need) {
+// still needed in it. Two block barriers.
+__device__ __forceinline__ void find_crossing(const int32_t* hist, int32_t need, ScanState& st, uint32_t* sh_digit,
+                                              int32_t* sh_need) {
     int32_t c[kBinsPerThread], s = 0;
 #pragma unroll
     for (int k = 0; k < kBinsPerThread; ++k) {
@@ -89,7 +90,7 @@ __device__ __forceinline__ void find_crossing(const int32_t* hist, int32_t need,
         s += c[k];
     }
     uint32_t total;
-    const int32_t above = static_cast<int32_t>(block_exclusive_scan(static_cast<uint32_t>(s), warp_sums, &total));
+    const int32_t above = static_cast<int32_t>(block_exclusive_scan(static_cast<uint32_t>(s), st, &total));
     if (above < need && above + s >= need) {
         int32_t acc = above;
 #pragma unroll
@@ -140,10 +141,9 @@ __device__ __forceinline__ void for_own_keys(const uint32_t* keys, int32_t base,
 
 __global__ void __launch_bounds__(kSelectThreads) select_staged_kernel(const SelectParams p) {
     extern __shared__ __align__(16) uint32_t keys[];  // [n_pools]
-    __shared__ int32_t hist[kBins];
+    __shared__ int32_t hist[2][kBins];                 // one digit counted while the other is cleared
     __shared__ uint32_t cand_key[kCandidates];
-    __shared__ uint32_t warp_sums[kSelectWarps];
-    __shared__ int32_t warp_cands[kSelectWarps];
+    __shared__ uint32_t scan_buf[2][kSelectWarps];
     __shared__ uint32_t sh_digit;
     __shared__ int32_t sh_need;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -154,12 +154,13 @@ __global__ void __launch_bounds__(kSelectThreads) select_staged_kernel(const Sel
     const int64_t by_pos = q < 0 ? 0 : (q + 1) / p.kpool;
     const int32_t n = static_cast<int32_t>(by_pos < p.n_pools ? by_pos : p.n_pools);  // eligible: pools [0, n)
     const int64_t width = static_cast<int64_t>(p.topk) * p.kpool;
+    ScanState st{scan_buf, 0};
 
     if (n <= p.topk) {  // every eligible pool is taken
         for (int64_t e = tid; e < width; e += kSelectThreads) out[e] = e < static_cast<int64_t>(n) * p.kpool ? static_cast<int32_t>(e) : -1;
         return;
     }
-    for (int b = tid; b < kBins; b += kSelectThreads) hist[b] = 0;
+    for (int b = tid; b < 2 * kBins; b += kSelectThreads) (&hist[0][0])[b] = 0;
     __syncthreads();
 
     // Stage the keys and count the first digit (bits 31..21), kLoadBatch loads in flight
@@ -181,29 +182,29 @@ __global__ void __launch_bounds__(kSelectThreads) select_staged_kernel(const Sel
             if (i < n4) {
                 const uint4 kk = make_uint4(score_key(v[k].x), score_key(v[k].y), score_key(v[k].z), score_key(v[k].w));
                 reinterpret_cast<uint4*>(keys)[i] = kk;
-                atomicAdd(&hist[kk.x >> 21], 1);
-                atomicAdd(&hist[kk.y >> 21], 1);
-                atomicAdd(&hist[kk.z >> 21], 1);
-                atomicAdd(&hist[kk.w >> 21], 1);
+                atomicAdd(&hist[0][kk.x >> 21], 1);
+                atomicAdd(&hist[0][kk.y >> 21], 1);
+                atomicAdd(&hist[0][kk.z >> 21], 1);
+                atomicAdd(&hist[0][kk.w >> 21], 1);
             }
         }
     }
     for (int32_t i = 4 * n4 + tid; i < n; i += kSelectThreads) {
         const uint32_t k = score_key(__ldg(sc + i));
         keys[i] = k;
-        atomicAdd(&hist[k >> 21], 1);
+        atomicAdd(&hist[0][k >> 21], 1);
     }
     __syncthreads();
-    find_crossing(hist, p.topk, warp_sums, &sh_digit, &sh_need);
+    find_crossing(hist[0], p.topk, st, &sh_digit, &sh_need);
     const uint32_t bin_lo = sh_digit << 21;  // keys of the threshold bin: [bin_lo, bin_lo + 2^21)
     int32_t need = sh_need;
+    for (int b = tid; b < kBins; b += kSelectThreads) hist[0][b] = 0;  // for the third digit
 
     // Candidates: the pools of the threshold bin. Thread t owns pools 32t .. 32t + 31 of
     // each round of kSelectThreads*32 pools; each warp lists its candidates in a region of
-    // its own (warp scan of the per-thread counts, no atomics).
+    // its own (warp scan of the per-thread counts, no atomics, no block barrier).
     const int32_t rounds = (n + kSelectThreads * 32 - 1) / (kSelectThreads * 32);
     int32_t my_cands = 0;  // this warp's, uniform over the warp
-    bool listed = true;
     for (int32_t rd = 0; rd < rounds; ++rd) {
         const int32_t base = rd * kSelectThreads * 32 + 32 * tid;
         uint32_t cmask = 0u;
@@ -229,33 +230,34 @@ __global__ void __launch_bounds__(kSelectThreads) select_staged_kernel(const Sel
             ++slot;
         }
     }
-    if (lane == 0) warp_cands[warp] = my_cands;
-    __syncthreads();
-#pragma unroll
-    for (int w = 0; w < kSelectWarps; ++w) listed = listed && warp_cands[w] <= kWarpCandidates;
+    __syncwarp();  // the warp's list, written by its lanes, is read by other lanes below
+    const bool listed = my_cands <= kWarpCandidates;  // per warp: else its own pools are re-read
+    const uint32_t* my_list = cand_key + warp * kWarpCandidates;
 
-    // The two last digits over the candidates (over every key of the bin when a warp's
-    // region overflowed).
+    // The two last digits: each warp counts its own candidates (or, when its list
+    // overflowed, the threshold-bin keys among its threads' own pools).
     uint32_t prefix = bin_lo, mask = 0x7FFu << 21;
 #pragma unroll 1
     for (int pass = 0; pass < 2; ++pass) {
         const int shift = pass == 0 ? 10 : 0;
         const uint32_t digit = pass == 0 ? 0x7FFu : 0x3FFu;
-        for (int b = tid; b < kBins; b += kSelectThreads) hist[b] = 0;
-        __syncthreads();
+        int32_t* h = hist[pass == 0 ? 1 : 0];
         if (listed) {
             for (int32_t j = lane; j < my_cands; j += 32) {
-                const uint32_t u = cand_key[warp * kWarpCandidates + j];
-                if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & digit], 1);
+                const uint32_t u = my_list[j];
+                if ((u & mask) == prefix) atomicAdd(&h[(u >> shift) & digit], 1);
             }
         } else {
-            for (int32_t j = tid; j < n; j += kSelectThreads) {
-                const uint32_t u = keys[j];
-                if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & digit], 1);
-            }
+            for (int32_t rd = 0; rd < rounds; ++rd)
+                for_own_keys(keys, rd * kSelectThreads * 32 + 32 * tid, n, [&](int, uint4 v, int valid) {
+                    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (e < valid && (u[e] & mask) == prefix) atomicAdd(&h[(u[e] >> shift) & digit], 1);
+                });
         }
         __syncthreads();
-        find_crossing(hist, need, warp_sums, &sh_digit, &sh_need);
+        find_crossing(h, need, st, &sh_digit, &sh_need);
         prefix |= sh_digit << shift;
         need = sh_need;
         mask |= digit << shift;
@@ -280,7 +282,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_staged_kernel(const Sel
         });
         uint32_t packed_total;
         const uint32_t packed =
-            block_exclusive_scan((static_cast<uint32_t>(__popc(emask)) << 16) | __popc(gmask), warp_sums, &packed_total);
+            block_exclusive_scan((static_cast<uint32_t>(__popc(emask)) << 16) | __popc(gmask), st, &packed_total);
         const int32_t left = max(0, need - eq_seen);  // equal pools still to take
         const int32_t eq_before = static_cast<int32_t>(packed >> 16);
         int32_t keep = min(__popc(emask), max(0, left - eq_before));
@@ -305,7 +307,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_staged_kernel(const Sel
 // then warp-segment compaction (see the file comment).
 __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectParams p) {
     __shared__ int32_t hist[kBins];
-    __shared__ uint32_t warp_sums[kSelectWarps];
+    __shared__ uint32_t scan_buf[2][kSelectWarps];
     __shared__ int32_t seg_out[kSelectWarps], seg_eq_base[kSelectWarps];
     __shared__ uint32_t sh_digit;
     __shared__ int32_t sh_need;
@@ -317,6 +319,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectPara
     const int64_t by_pos = q < 0 ? 0 : (q + 1) / p.kpool;
     const int32_t n = static_cast<int32_t>(by_pos < p.n_pools ? by_pos : p.n_pools);  // eligible: pools [0, n)
     const int64_t width = static_cast<int64_t>(p.topk) * p.kpool;
+    ScanState st{scan_buf, 0};
     if (n <= p.topk) {  // every eligible pool is taken
         for (int64_t e = tid; e < width; e += kSelectThreads) out[e] = e < static_cast<int64_t>(n) * p.kpool ? static_cast<int32_t>(e) : -1;
         return;
@@ -336,7 +339,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectPara
             if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & digit], 1);
         }
         __syncthreads();
-        find_crossing(hist, need, warp_sums, &sh_digit, &sh_need);
+        find_crossing(hist, need, st, &sh_digit, &sh_need);
         prefix |= sh_digit << shift;
         need = sh_need;
         mask |= digit << shift;
@@ -354,9 +357,9 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectPara
         eq += __popc(__ballot_sync(0xffffffffu, i < hi && u == prefix));
     }
     uint32_t eq_total, t_total;
-    const int32_t e_base = static_cast<int32_t>(block_exclusive_scan(lane == 0 ? eq : 0, warp_sums, &eq_total));
+    const int32_t e_base = static_cast<int32_t>(block_exclusive_scan(lane == 0 ? eq : 0, st, &eq_total));
     const int32_t t = gt + max(0, min(eq, need - e_base));
-    const int32_t t_base = static_cast<int32_t>(block_exclusive_scan(lane == 0 ? t : 0, warp_sums, &t_total));
+    const int32_t t_base = static_cast<int32_t>(block_exclusive_scan(lane == 0 ? t : 0, st, &t_total));
     if (lane == 0) {
         seg_out[warp] = t_base;
         seg_eq_base[warp] = e_base;
