@@ -12,6 +12,8 @@ source pages it restates:
 * ``attend.rs`` = spark_model/layers/glm5next_dsa/attend.rs
 * ``decode_k.rs`` = metrale_model_arch/glm5next_dsa/layer/decode_k.rs
 
+* ``build.rs`` = spark_model/layers/glm5next_dsa/build.rs
+
 The cache writer (``latent_write``, ``e4m3_encode``) restates the ``latent_write`` launch
 of decode_k.rs ``decode_k``; its kernel body is not on the pages and the reading taken is
 written beside ``oracle_latent_write`` in ``dsa_oracle.c``.
@@ -70,6 +72,9 @@ def _bind(path: str):
     lib.oracle_latent_write.restype = i32
     lib.oracle_select_pools.argtypes = [P, P, i32, i32, i32, i32, P]
     lib.oracle_select_pools.restype = i32
+    for name in ("oracle_absorb_q", "oracle_absorb_o"):
+        getattr(lib, name).argtypes = [P, P, i32, i32, i32, i32, i32, i64, i64, P]
+        getattr(lib, name).restype = i32
     return lib
 
 
@@ -221,4 +226,45 @@ def select_pools(scores, q_pos, kpool: int, topk: int, lib=None) -> np.ndarray:
     rc = (lib or _load()).oracle_select_pools(_ptr(sc), _ptr(qp), rows, n_pools, int(kpool), int(topk), _ptr(out))
     if rc != 0:
         raise ValueError("oracle_select_pools: bad arguments")
+    return out
+
+
+def _bf16_bits(a) -> np.ndarray:
+    a = np.asarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError("BF16 inputs are passed as uint16 bit patterns")
+    return np.ascontiguousarray(a)
+
+
+def absorb_q(q_b, kv_b, heads: int, nope: int, vd: int, kvl: int = LATENT, rows=None, lib=None) -> np.ndarray:
+    """build.rs ``absorb_q``: q_absorb[h*kvl + c, k] = sum_r kv_b[h*(nope+vd) + r, c] *
+    q_b[h*nope + r, k] in float64. q_b: BF16 bits [heads*nope, ql]; kv_b: BF16 bits
+    [heads*(nope+vd), kvl]. rows=(row0, nrows) computes only those output rows.
+    Returns float64 [nrows, ql]."""
+    qb, kb = _bf16_bits(q_b), _bf16_bits(kv_b)
+    ql = qb.shape[1]
+    if qb.shape != (heads * nope, ql) or kb.shape != (heads * (nope + vd), kvl):
+        raise ValueError("absorb_q: shapes do not match heads/nope/vd/kvl")
+    row0, nrows = rows if rows is not None else (0, heads * kvl)
+    out = np.empty((nrows, ql), dtype=np.float64)
+    rc = (lib or _load()).oracle_absorb_q(_ptr(qb), _ptr(kb), heads, nope, vd, kvl, ql, row0, nrows, _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_absorb_q: bad arguments")
+    return out
+
+
+def absorb_o(o_proj, kv_b, heads: int, nope: int, vd: int, kvl: int = LATENT, rows=None, lib=None) -> np.ndarray:
+    """build.rs ``absorb_o``: o_absorb[i, h*kvl + c] = sum_r o_proj[i, h*vd + r] *
+    kv_b[h*(nope+vd) + nope + r, c] in float64 (the V half of kv_b). o_proj: BF16 bits
+    [hidden, heads*vd]; kv_b as for absorb_q. rows=(row0, nrows) computes only those
+    output rows. Returns float64 [nrows, heads*kvl]."""
+    op, kb = _bf16_bits(o_proj), _bf16_bits(kv_b)
+    hidden = op.shape[0]
+    if op.shape != (hidden, heads * vd) or kb.shape != (heads * (nope + vd), kvl):
+        raise ValueError("absorb_o: shapes do not match heads/nope/vd/kvl")
+    row0, nrows = rows if rows is not None else (0, hidden)
+    out = np.empty((nrows, heads * kvl), dtype=np.float64)
+    rc = (lib or _load()).oracle_absorb_o(_ptr(op), _ptr(kb), heads, nope, vd, kvl, hidden, row0, nrows, _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_absorb_o: bad arguments")
     return out

@@ -408,3 +408,54 @@ int32_t oracle_select_pools(const float* scores, const int32_t* q_pos, int32_t r
     free(taken);
     return 0;
 }
+
+/* ------------------------------------------------------------------------------------
+ * Load-time transforms of absorbed MLA.
+ *
+ * [build.rs] absorb_q: the query up-projection q_b is pre-multiplied by the K half of
+ * kv_b, so that queries arrive in the kvl-dim latent space the decode dots against:
+ *   q_absorb[h*kvl + c][k] = sum_{r < nope} kv_b[h*(nope+vd) + r][c] * q_b[h*nope + r][k]
+ * with q_b [heads*nope, ql], kv_b [heads*(nope+vd), kvl], q_absorb [heads*kvl, ql].
+ * [build.rs] absorb_o: the output projection is pre-multiplied by the V half of kv_b
+ * (rows nope .. nope+vd-1 of each head's block), so that it reads the decode's latent
+ * output:
+ *   o_absorb[i][h*kvl + c] = sum_{r < vd} o_proj[i][h*vd + r] * kv_b[h*(nope+vd) + nope + r][c]
+ * with o_proj [hidden, heads*vd], o_absorb [hidden, heads*kvl]. All matrices row-major;
+ * NoPE (no rope section, [build.rs] absorb_q refuses one). Inputs are the checkpoint's
+ * BF16 values; the sums are in double. Only output rows [row0, row0 + nrows) are written
+ * (out points at row row0), so a large transform can be checked on sampled rows.
+ * ---------------------------------------------------------------------------------- */
+
+int32_t oracle_absorb_q(const uint16_t* q_b, const uint16_t* kv_b, int32_t heads, int32_t nope, int32_t vd,
+                        int32_t kvl, int32_t ql, int64_t row0, int64_t nrows, double* out) {
+    if (heads < 1 || nope < 1 || vd < 0 || kvl < 1 || ql < 1) return -1;
+    if (row0 < 0 || nrows < 0 || row0 + nrows > (int64_t)heads * kvl) return -1;
+    for (int64_t row = row0; row < row0 + nrows; ++row) {
+        const int64_t h = row / kvl, c = row % kvl;
+        for (int64_t k = 0; k < ql; ++k) {
+            double sum = 0.0;
+            for (int64_t r = 0; r < nope; ++r)
+                sum += oracle_bf16_to_f64(kv_b[(h * (nope + vd) + r) * kvl + c]) *
+                       oracle_bf16_to_f64(q_b[(h * nope + r) * ql + k]);
+            out[(row - row0) * ql + k] = sum;
+        }
+    }
+    return 0;
+}
+
+int32_t oracle_absorb_o(const uint16_t* o_proj, const uint16_t* kv_b, int32_t heads, int32_t nope, int32_t vd,
+                        int32_t kvl, int32_t hidden, int64_t row0, int64_t nrows, double* out) {
+    if (heads < 1 || nope < 0 || vd < 1 || kvl < 1 || hidden < 1) return -1;
+    if (row0 < 0 || nrows < 0 || row0 + nrows > hidden) return -1;
+    const int64_t in_w = (int64_t)heads * vd, out_w = (int64_t)heads * kvl;
+    for (int64_t i = row0; i < row0 + nrows; ++i)
+        for (int64_t h = 0; h < heads; ++h)
+            for (int64_t c = 0; c < kvl; ++c) {
+                double sum = 0.0;
+                for (int64_t r = 0; r < vd; ++r)
+                    sum += oracle_bf16_to_f64(o_proj[i * in_w + h * vd + r]) *
+                           oracle_bf16_to_f64(kv_b[(h * (nope + vd) + nope + r) * kvl + c]);
+                out[(i - row0) * out_w + h * kvl + c] = sum;
+            }
+    return 0;
+}
