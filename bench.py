@@ -592,6 +592,42 @@ def run_select(args):
             "roofline": _hbm_roofline(nbytes, us)}
 
 
+def run_absorb(args):
+    """Times dsa_absorb_q and dsa_absorb_o (FP32 out) at the model size the pages' widths
+    give: 64 heads, nope = vd = 256, kvl 512, q_lora_rank 2048, hidden 6144. Each is a
+    batched BF16 GEMM; its roofline is the larger of its bytes (weights read, FP32 result
+    written) over measured HBM and its flops over the measured dense BF16 peak. At K = 256
+    both are HBM-bound (about 93 flops per byte)."""
+    import sparse_mla_paged_gb300.api as api
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    H, nope, vd, kvl, ql, hidden = 64, 256, 256, 512, 2048, 6144
+    q_b, kv_b, o_proj = wl.absorb_weights(H, nope, vd, kvl, ql, hidden, device=device)
+    qa = torch.empty((H * kvl, ql), dtype=torch.float32, device=device)
+    oa = torch.empty((hidden, H * kvl), dtype=torch.float32, device=device)
+    stream = torch.cuda.Stream(device)
+    peaks, _ = load_peaks()
+    hbm, tensor = float(peaks["hbm_gbs"]), float(peaks["bf16_tflops"])
+    res = {"component": "absorb", "heads": H, "nope": nope, "vd": vd, "kvl": kvl, "q_lora_rank": ql,
+           "hidden": hidden, "unit": "us/call"}
+    cases = (("absorb_q", lambda i: api.absorb_q(q_b, kv_b, H, nope, vd, out=qa, stream=stream),
+              2.0 * H * kvl * ql * nope, 2 * H * nope * ql + 2 * H * nope * kvl + 4 * H * kvl * ql),
+             ("absorb_o", lambda i: api.absorb_o(o_proj, kv_b, H, nope, vd, out=oa, stream=stream),
+              2.0 * hidden * H * kvl * vd, 2 * hidden * H * vd + 2 * H * vd * kvl + 4 * hidden * H * kvl))
+    for name, call, flops, nbytes in cases:
+        us, calls = _time_in_graphs(call, min(args.steps, 512), args.warmup, stream)
+        t_hbm, t_tensor = nbytes / (hbm * 1e3), flops / (tensor * 1e6)  # microseconds
+        if t_hbm >= t_tensor:
+            roof = {"bound": "hbm", "achieved": round(nbytes / (us * 1e3), 1), "peak": hbm, "unit": "GB/s"}
+        else:
+            roof = {"bound": "tensor", "achieved": round(flops / (us * 1e6), 1), "peak": tensor, "unit": "TFLOP/s"}
+        roof["frac"] = round(max(t_hbm, t_tensor) / us, 4)
+        res[name] = {"value": round(us, 2), "calls": calls, "flops_per_call": flops, "bytes_per_call": nbytes,
+                     "tensor_tflops": round(flops / (us * 1e6), 1), "roofline": roof}
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -613,7 +649,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
-    ap.add_argument("--component", choices=["latent_write", "select"], default=None,
+    ap.add_argument("--component", choices=["latent_write", "select", "absorb"], default=None,
                     help="time one component of the path instead of the decode step (its own JSON line)")
     ap.add_argument("--rows", type=int, default=128, help="rows per call for --component latent_write / select")
     ap.add_argument("--traffic", type=float, default=None,
@@ -631,7 +667,8 @@ def main():
         print(json.dumps({"metric": METRIC, "error": "no CUDA device"}))
         return 1
     if args.component is not None:
-        print(json.dumps({"latent_write": run_latent_write, "select": run_select}[args.component](args)))
+        print(json.dumps({"latent_write": run_latent_write, "select": run_select,
+                          "absorb": run_absorb}[args.component](args)))
         return 0
     init_dist(ws_n, "nccl")
     line = run_cuda(args, ws_n, rank, local)

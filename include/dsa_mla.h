@@ -262,6 +262,28 @@ int32_t dsa_select_pools(const float* scores, const int32_t* q_pos, int32_t rows
                          void* stream);
 
 /*
+ * dsa_absorb_q, dsa_absorb_o: the load-time transforms of absorbed MLA (build.rs,
+ * absorb_q and absorb_o), the pair that puts the decode's queries and outputs in the
+ * kv_lora_rank-dim latent space (NoPE: no rope section). All matrices row-major, BF16
+ * weights as the checkpoint stores them, FP32 accumulation on the tensor cores (cuBLAS),
+ * output FP32 (out_dtype 0) or BF16 rounded to nearest even (out_dtype 1):
+ *   q_absorb[h*kvl + c][k] = sum_{r < nope} kv_b[h*(nope+vd) + r][c] * q_b[h*nope + r][k]
+ *   o_absorb[i][h*kvl + c] = sum_{r < vd} o_proj[i][h*vd + r] * kv_b[h*(nope+vd) + nope + r][c]
+ *  q_b     bf16 [heads*nope, q_lora_rank]   (the query up-projection, per head nope rows)
+ *  kv_b    bf16 [heads*(nope+vd), kvl]      (per head: nope K rows, then vd V rows)
+ *  o_proj  bf16 [hidden, heads*vd]          (the output projection)
+ *  out     [heads*kvl, q_lora_rank] for absorb_q, [hidden, heads*kvl] for absorb_o;
+ *          caller-owned device memory, 4-byte (FP32) or 2-byte (BF16) aligned.
+ *  heads, nope, vd, kvl, q_lora_rank, hidden >= 1; heads*(nope+vd), heads*kvl and
+ *  heads*vd below 2^31 (DSA_ERR_UNSUPPORTED otherwise). Inputs 2-byte aligned.
+ * Enqueued on `stream`; returns DSA_ERR_CUDA when the library GEMM fails.
+ */
+int32_t dsa_absorb_q(const void* q_b, const void* kv_b, int32_t heads, int32_t nope, int32_t vd,
+                     int32_t kvl, int32_t q_lora_rank, void* out, int32_t out_dtype, void* stream);
+int32_t dsa_absorb_o(const void* o_proj, const void* kv_b, int32_t heads, int32_t nope, int32_t vd,
+                     int32_t kvl, int32_t hidden, void* out, int32_t out_dtype, void* stream);
+
+/*
  * dsa_mla_decode_static: dsa_mla_decode for callers that cannot allocate device memory at
  * call time (for instance code running under a framework that owns all device memory
  * through its own pool, or a latency-critical path that cannot accept cudaMalloc's

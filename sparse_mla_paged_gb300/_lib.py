@@ -49,6 +49,8 @@ SIGNATURES = {
     "dsa_resolve_indices": ([_P, _P, _I32, _I32, _P, _P, _P], _I32),
     "dsa_latent_write": ([_P, _P, _P, _I32, _F32, _F32, _I32, _I64, _P, _P], _I32),
     "dsa_select_pools": ([_P, _P, _I32, _I32, _I32, _I32, _P, _P], _I32),
+    "dsa_absorb_q": ([_P, _P, _I32, _I32, _I32, _I32, _I32, _P, _I32, _P], _I32),
+    "dsa_absorb_o": ([_P, _P, _I32, _I32, _I32, _I32, _I32, _P, _I32, _P], _I32),
     "dsa_read_device_status": ([_P, _P, _P], _I32),
     "dsa_last_device_status": ([_P, _P], _I32),
     "dsa_static_device_status": ([_P, _P], _I32),

@@ -188,6 +188,47 @@ def select_pools(scores: torch.Tensor, q_pos: torch.Tensor, kpool: int, topk: in
     return out
 
 
+def _absorb_out(shape, dtype, device, out):
+    if dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("absorb output must be float32 or bfloat16")
+    if out is None:
+        out = torch.empty(shape, dtype=dtype, device=device)
+    _need(out, dtype, "out")
+    if tuple(out.shape) != tuple(shape):
+        raise ValueError(f"out must have shape {tuple(shape)}")
+    return out, 0 if dtype == torch.float32 else 1
+
+
+def absorb_q(q_b: torch.Tensor, kv_b: torch.Tensor, heads: int, nope: int, vd: int, dtype=torch.float32, out=None,
+             stream=None) -> torch.Tensor:
+    """dsa_absorb_q (build.rs absorb_q): q_b bf16 [heads*nope, q_lora_rank], kv_b bf16
+    [heads*(nope+vd), kvl] -> [heads*kvl, q_lora_rank] in `dtype` (float32 or bfloat16)."""
+    _need(q_b, torch.bfloat16, "q_b")
+    _need(kv_b, torch.bfloat16, "kv_b")
+    ql, kvl = q_b.shape[1], kv_b.shape[1]
+    if q_b.shape[0] != heads * nope or kv_b.shape[0] != heads * (nope + vd):
+        raise ValueError("absorb_q: shapes do not match heads/nope/vd")
+    out, code = _absorb_out((heads * kvl, ql), dtype, q_b.device, out)
+    check(_lib.load().dsa_absorb_q(_ptr(q_b), _ptr(kv_b), heads, nope, vd, kvl, ql, _ptr(out), code,
+                                   _stream(stream)), "dsa_absorb_q")
+    return out
+
+
+def absorb_o(o_proj: torch.Tensor, kv_b: torch.Tensor, heads: int, nope: int, vd: int, dtype=torch.float32,
+             out=None, stream=None) -> torch.Tensor:
+    """dsa_absorb_o (build.rs absorb_o): o_proj bf16 [hidden, heads*vd], kv_b bf16
+    [heads*(nope+vd), kvl] -> [hidden, heads*kvl] in `dtype` (float32 or bfloat16)."""
+    _need(o_proj, torch.bfloat16, "o_proj")
+    _need(kv_b, torch.bfloat16, "kv_b")
+    hidden, kvl = o_proj.shape[0], kv_b.shape[1]
+    if o_proj.shape[1] != heads * vd or kv_b.shape[0] != heads * (nope + vd):
+        raise ValueError("absorb_o: shapes do not match heads/nope/vd")
+    out, code = _absorb_out((hidden, heads * kvl), dtype, o_proj.device, out)
+    check(_lib.load().dsa_absorb_o(_ptr(o_proj), _ptr(kv_b), heads, nope, vd, kvl, hidden, _ptr(out), code,
+                                   _stream(stream)), "dsa_absorb_o")
+    return out
+
+
 def read_device_status(workspace: torch.Tensor, stream=None) -> int:
     v = _lib.ctypes.c_int32(0)
     check(_lib.load().dsa_read_device_status(_ptr(workspace), _lib.ctypes.byref(v), _stream(stream)),

@@ -1,7 +1,8 @@
 """In-tree build of libdsa_mla.so (sm_103a) with nvcc.
 
 Each translation unit under csrc/ is compiled in parallel to an object in _build/, then
-linked into sparse_mla_paged_gb300/libdsa_mla.so against the shared CUDA runtime.
+linked into sparse_mla_paged_gb300/libdsa_mla.so against the shared CUDA runtime (and
+cuBLAS, for the load-time absorb GEMMs).
 """
 from __future__ import annotations
 
@@ -16,12 +17,13 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdsa_mla.so")
-SOURCES = ["api.cu", "prologue.cu", "decode.cu", "combine.cu", "static_scratch.cu", "latent_write.cu", "select.cu"]
+SOURCES = ["api.cu", "prologue.cu", "decode.cu", "combine.cu", "static_scratch.cu", "latent_write.cu", "select.cu",
+           "absorb.cu"]
 # Translation units: (source, object, extra flags); decode.cu is built once per tile size.
 UNITS = [("api.cu", "api.o", []), ("prologue.cu", "prologue.o", []),
          ("decode.cu", "decode64.o", ["-DDSA_TILE=64"]), ("decode.cu", "decode128.o", ["-DDSA_TILE=128"]),
          ("combine.cu", "combine.o", []), ("static_scratch.cu", "static_scratch.o", []),
-         ("latent_write.cu", "latent_write.o", []), ("select.cu", "select.o", [])]
+         ("latent_write.cu", "latent_write.o", []), ("select.cu", "select.o", []), ("absorb.cu", "absorb.o", [])]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -64,7 +66,7 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     with cf.ThreadPoolExecutor(max_workers=len(UNITS)) as ex:
         objs = list(ex.map(lambda u: _compile(u, extra), UNITS))
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs]
+    cmd = [nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs, "-lcublas"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

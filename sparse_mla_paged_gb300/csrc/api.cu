@@ -365,6 +365,12 @@ Args make_args(const void* q, const void* k_cache, const void* v_cache, const in
 
 }  // namespace
 
+// The device check shared with the other translation units (the absorb transforms).
+int32_t dsa::check_device() {
+    DeviceState* d = nullptr;
+    return current_device(&d);
+}
+
 extern "C" {
 
 #ifdef DSA_TRACE

@@ -229,6 +229,7 @@ cudaError_t launch_decode_128(const DecodeParams& p, const CUtensorMap& kmap, co
 // max_pieces: the most CTAs sharing one unit (max_pieces_per_unit; selects the variant).
 cudaError_t launch_combine(const CombineParams& p, int units, int max_pieces, cudaStream_t stream);
 cudaError_t launch_latent_write(const LatentWriteParams& p, cudaStream_t stream);
+int32_t check_device();  // DSA_OK when the current device is an sm_103 with the kernels loaded
 cudaError_t select_kernel_setup();
 cudaError_t launch_select(const SelectParams& p, cudaStream_t stream);
 cudaError_t decode_kernel_setup_64();

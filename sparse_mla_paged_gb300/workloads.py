@@ -395,3 +395,17 @@ def flat_tail(*, heads=64, width=2048, tail_value=20.0, dominant_at=("first", "m
     return Workload(f"flat tail: {S} seqs x {heads} heads, width {width}, gaps {gap_lo}..{gap_hi}", q, cache,
                     None, bt, torch.full((S,), width, dtype=torch.int32, device=device), sel, S, 1, heads, bs,
                     bs * LATENT, pages, 1.0 / 448.0, 0.05, math.log(2.0))
+
+
+def absorb_weights(heads: int = 64, nope: int = 256, vd: int = 256, kvl: int = LATENT, q_lora_rank: int = 2048,
+                   hidden: int = 6144, device="cpu", seed: Optional[int] = None):
+    """Synthetic BF16 weights for the load-time absorb transforms (the checkpoint's are not
+    on the pages): q_b [heads*nope, q_lora_rank], kv_b [heads*(nope+vd), kvl] and o_proj
+    [hidden, heads*vd], each N(0, 1/fan_in). Defaults: 64 heads, nope = vd = 256
+    (qk_head_dim 256 and nope + v_head_dim 512 as the pages state), kvl 512, q_lora_rank
+    2048, hidden 6144."""
+    g = _gen(device, BASE_SEED + 11 if seed is None else seed)
+
+    def w(rows, cols):
+        return (torch.randn((rows, cols), generator=g, device=device) / math.sqrt(cols)).to(torch.bfloat16)
+    return w(heads * nope, q_lora_rank), w(heads * (nope + vd), kvl), w(hidden, heads * vd)

@@ -26,7 +26,7 @@ def test_header_declares_expected_entry_points():
     names = _declared_functions()
     for want in ("dsa_mla_decode", "dsa_mla_decode_k", "dsa_mla_decode_ws", "dsa_resolve_indices",
                  "dsa_mla_decode_workspace_bytes", "dsa_status_string", "dsa_read_device_status",
-                 "dsa_mla_decode_host", "dsa_latent_write", "dsa_select_pools"):
+                 "dsa_mla_decode_host", "dsa_latent_write", "dsa_select_pools", "dsa_absorb_q", "dsa_absorb_o"):
         assert want in names
 
 
@@ -152,3 +152,17 @@ def test_select_rejects_bad_arguments_on_host(lib):
     assert call(n=1 << 30, kpool=4) == 2            # token ids would pass 2^31
     assert call(topk=1 << 29, kpool=8) == 2
     assert call(rows=0, sc=0, q=0, ids=0) == 0       # nothing to select: no device needed
+
+
+def test_absorb_rejects_bad_arguments_on_host(lib):
+    for f in (lib.dsa_absorb_q, lib.dsa_absorb_o):
+        ok = dict(a=0x10000, kv=0x20000, heads=4, nope=64, vd=64, kvl=512, other=256, out=0x30000, dt=0)
+
+        def call(**over):
+            a = dict(ok, **over)
+            return f(a["a"], a["kv"], a["heads"], a["nope"], a["vd"], a["kvl"], a["other"], a["out"], a["dt"], None)
+
+        for over in (dict(a=0), dict(kv=0), dict(out=0), dict(heads=0), dict(nope=0), dict(vd=0), dict(kvl=0),
+                     dict(other=0), dict(dt=2), dict(dt=-1), dict(a=0x10001), dict(kv=0x20001), dict(out=0x30002)):
+            assert call(**over) == 1, over
+        assert call(heads=1 << 20, nope=1 << 11, vd=1 << 11) == 2     # heads*(nope+vd) past int
