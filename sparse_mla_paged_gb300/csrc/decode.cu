@@ -62,6 +62,7 @@ constexpr int kThreads = (kSoftmaxWarp0 + kSoftmaxWarps) * 32;  // 384: 3 warps 
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
 
 constexpr int kBarSoftmax = 1;  // named barrier over the softmax warps
+constexpr int kBarPair0 = 2;    // 2..5: the two softmax warps of TMEM lane quarter q (64 threads)
 
 // Operand layout of a tile: token tk at (tk/8)*4096 + kb*1024 + (tk%8)*128 for its
 // 128-dim block kb, 16-byte chunks of each 128-byte row permuted by tk%8 (128-byte
@@ -77,8 +78,8 @@ static_assert(kSlotsKV <= 6 && kSBufs >= 1 && kScores % 16 == 0, "tile geometry"
 constexpr int kOffRing = 0;
 constexpr int kOffP = kOffRing + kRingBytes;                     // P' [2 buffers][hi, lo]; epilogue staging
 constexpr int kOffHm = kOffP + 4 * kPTermBytes;                  // float [2 token halves][64] tile maxima
-constexpr int kOffAlpha = kOffHm + 2 * kHeadsPerCta * 4;         // float [64] rescale factors
-constexpr int kOffL = kOffAlpha + kHeadsPerCta * 4;              // float [2 token halves][64] row sums
+constexpr int kOffAlpha = kOffHm + 2 * kHeadsPerCta * 4;         // float [2 tile parities][64] rescale factors
+constexpr int kOffL = kOffAlpha + 2 * kHeadsPerCta * 4;          // float [2 token halves][64] row sums
 constexpr int kOffF = kOffL + 2 * kHeadsPerCta * 4;              // float [64] output factors
 constexpr int kOffBars = kOffF + kHeadsPerCta * 4;
 enum {
@@ -650,44 +651,48 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
             }
 #pragma unroll
             for (int j = 0; j < kScores; ++j) hm4[j & 3] = fmaxf(hm4[j & 3], x[j]);
-            // Max of head hq over this warp's half of the tile.
+            // Max of head hq over the tile: this warp's half (both term lanes), then the
+            // other half from the partner warp of the lane quarter (64-thread barrier; the
+            // buffer is rewritten only after the block barrier below, which the partner
+            // passes after reading it).
             float hmax = fmaxf(fmaxf(hm4[0], hm4[1]), fmaxf(hm4[2], hm4[3]));
             hmax = fmaxf(hmax, __shfl_xor_sync(0xffffffffu, hmax, 1));
-            const bool over = hmax > m_ref + kRescaleMargin;
-            const bool under = hmax < m_ref - kRescaleDrop && m_ref > m_top - kRescaleFloor;
-            const bool any_change = named_bar_any<kBarSoftmax, kSoftmaxThreads>(over || under);
+            if (term == 0) hm_s[half * kHeadsPerCta + hq] = hmax;
+            named_bar_sync_id(kBarPair0 + q4, 64);
+            const float tm = fmaxf(hm_s[hq], hm_s[kHeadsPerCta + hq]);
             if (st == 0 && (tau == 2 || tau == 3)) DSA_TRACE_AT(p, 73 + 8 * (tau - 2));
-            // 32-head blocks of O^T that need rescaling before this tile's P.V (uniform).
-            bool resc[2] = {false, false};
-            if (any_change) {
-                // Reset the reference of every head whose tile max exceeds it by more than
-                // the margin, or lies more than kRescaleDrop below it; O and the row sums
-                // are rescaled by 2^(m_old - m_new).
-                if (term == 0) hm_s[half * kHeadsPerCta + hq] = hmax;
-                named_bar_sync<kBarSoftmax, kSoftmaxThreads>();
-                if (st == 0 && (tau == 2 || tau == 3)) DSA_TRACE_AT(p, 77 + 8 * (tau - 2));
-                const float tm = fmaxf(hm_s[hq], hm_s[kHeadsPerCta + hq]);
-                float m_new = m_ref;
-                if (tm > m_ref + kRescaleMargin || (tm < m_ref - kRescaleDrop && m_ref > m_top - kRescaleFloor))
-                    m_new = fmaxf(tm + kRescaleSlack, m_top - kRescaleFloor);
-                const float alpha = m_ref == kNegInf ? 0.0f : ex2_approx(m_ref - m_new);
+            // Reset the reference of head hq when the tile max exceeds it by more than the
+            // margin, or lies more than kRescaleDrop below it; O and the row sums are
+            // rescaled by 2^(m_old - m_new). Every thread of the head's pair computes the
+            // same values; the factors are published (double-buffered by tile parity: a
+            // buffer is rewritten two tiles later, after every reader passed the next
+            // block barrier) and one block barrier tells every warp whether any changed.
+            const bool change = tm > m_ref + kRescaleMargin || (tm < m_ref - kRescaleDrop && m_ref > m_top - kRescaleFloor);
+            float alpha = 1.0f;
+            if (change) {
+                const float m_new = fmaxf(tm + kRescaleSlack, m_top - kRescaleFloor);
+                alpha = m_ref == kNegInf ? 0.0f : ex2_approx(m_ref - m_new);
                 l_part *= alpha;
                 m_ref = m_new;
                 m_top = fmaxf(m_top, m_new);
-                if (term == 0 && half == 0) alpha_s[hq] = alpha;
-                named_bar_sync<kBarSoftmax, kSoftmaxThreads>();
-                if (t > 0) {
-                    // Blocks of 32 heads whose factors are all 1 are left alone.
+            }
+            const float* alpha_t = alpha_s + (tau & 1) * kHeadsPerCta;
+            if (term == 0 && half == 0) alpha_s[(tau & 1) * kHeadsPerCta + hq] = alpha;
+            const bool any_change = named_bar_any<kBarSoftmax, kSoftmaxThreads>(change);
+            if (st == 0 && (tau == 2 || tau == 3)) DSA_TRACE_AT(p, 77 + 8 * (tau - 2));
+            // 32-head blocks of O^T that need rescaling before this tile's P.V (uniform).
+            bool resc[2] = {false, false};
+            if (any_change && t > 0) {
+                // Blocks of 32 heads whose factors are all 1 are left alone.
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        bool ch = false;
+                for (int hh = 0; hh < 2; ++hh) {
+                    bool ch = false;
 #pragma unroll
-                        for (int h = 0; h < 32; h += 4) {
-                            const float4 a4 = *reinterpret_cast<const float4*>(alpha_s + hh * 32 + h);
-                            ch |= (a4.x != 1.0f) | (a4.y != 1.0f) | (a4.z != 1.0f) | (a4.w != 1.0f);
-                        }
-                        resc[hh] = ch;
+                    for (int h = 0; h < 32; h += 4) {
+                        const float4 a4 = *reinterpret_cast<const float4*>(alpha_t + hh * 32 + h);
+                        ch |= (a4.x != 1.0f) | (a4.y != 1.0f) | (a4.z != 1.0f) | (a4.w != 1.0f);
                     }
+                    resc[hh] = ch;
                 }
             }
 
@@ -737,7 +742,7 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
                         tmem_ld_x32(ta, o);
 #pragma unroll
                         for (int k = 0; k < 32; ++k)
-                            o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha_s[hh * 32 + k]);
+                            o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha_t[hh * 32 + k]);
                         tmem_st_x32(ta, o);
                     }
                 }

@@ -168,6 +168,12 @@ __device__ __forceinline__ void named_bar_sync() {
     asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(N) : "memory");
 }
 
+// Named barrier with a run-time ID (1..15) over n threads (whole warps).
+__device__ __forceinline__ void named_bar_sync_id(uint32_t id, uint32_t n) {
+    __syncwarp();
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // Named barrier ID over N threads that also returns whether `pred` held in any of them.
 template <int ID, int N>
 __device__ __forceinline__ bool named_bar_any(bool pred) {
