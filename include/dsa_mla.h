@@ -5,6 +5,7 @@
  * Source pages (cited by title and item):
  *   [attend.rs]   spark_model/layers/glm5next_dsa/attend.rs
  *   [decode_k.rs] metrale_model_arch/glm5next_dsa/layer/decode_k.rs
+ *   [build.rs]    spark_model/layers/glm5next_dsa/build.rs (the load-time absorb transforms)
  *
  * What is computed (attend.rs, module doc and decode_attention). For every decode row r
  * (sequence seq = r / rows_per_seq) and query head h:

@@ -81,7 +81,8 @@ constexpr int kOffHm = kOffP + 4 * kPTermBytes;                  // float [2 tok
 constexpr int kOffAlpha = kOffHm + 2 * kHeadsPerCta * 4;         // float [2 tile parities][64] rescale factors
 constexpr int kOffL = kOffAlpha + 2 * kHeadsPerCta * 4;          // float [2 token halves][64] row sums
 constexpr int kOffF = kOffL + 2 * kHeadsPerCta * 4;              // float [64] output factors
-constexpr int kOffBars = kOffF + kHeadsPerCta * 4;
+constexpr int kOffFlags = kOffF + kHeadsPerCta * 4;              // u32 [2 tile parities][4 lane quarters]
+constexpr int kOffBars = kOffFlags + 2 * 4 * 4;
 enum {
     BAR_FULL0 = 0,    // 6: ring slot gathered
     BAR_EMPTY0 = 6,   // 6: ring slot free again (its P.V is done)
@@ -556,6 +557,7 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
     float* alpha_s = reinterpret_cast<float*>(smem + kOffAlpha);
     float* l_s = reinterpret_cast<float*>(smem + kOffL);
     float* f_s = reinterpret_cast<float*>(smem + kOffF);
+    uint32_t* flag_s = reinterpret_cast<uint32_t*>(smem + kOffFlags);
     static_assert(kSoftmaxWarps * 2048 <= 4 * kPTermBytes, "epilogue staging fits the P buffers");
     uint8_t* stage = smem + kOffP + sw * 2048;  // epilogue staging (2 KB per warp)
     auto barp = [&](int b) { return sbase + kOffBars + 8 * b; };
@@ -678,22 +680,18 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
             }
             const float* alpha_t = alpha_s + (tau & 1) * kHeadsPerCta;
             if (term == 0 && half == 0) alpha_s[(tau & 1) * kHeadsPerCta + hq] = alpha;
+            // Which of this lane quarter's 16 heads changed (both warps of the pair agree).
+            const uint32_t changed = __ballot_sync(0xffffffffu, change);
+            if (half == 0 && lane == 0) flag_s[(tau & 1) * 4 + q4] = changed;
             const bool any_change = named_bar_any<kBarSoftmax, kSoftmaxThreads>(change);
             if (st == 0 && (tau == 2 || tau == 3)) DSA_TRACE_AT(p, 77 + 8 * (tau - 2));
-            // 32-head blocks of O^T that need rescaling before this tile's P.V (uniform).
+            // 32-head blocks of O^T that need rescaling before this tile's P.V: heads 0-31
+            // live in lane quarters 0-1, heads 32-63 in 2-3 (uniform over the softmax warps).
             bool resc[2] = {false, false};
             if (any_change && t > 0) {
-                // Blocks of 32 heads whose factors are all 1 are left alone.
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    bool ch = false;
-#pragma unroll
-                    for (int h = 0; h < 32; h += 4) {
-                        const float4 a4 = *reinterpret_cast<const float4*>(alpha_t + hh * 32 + h);
-                        ch |= (a4.x != 1.0f) | (a4.y != 1.0f) | (a4.z != 1.0f) | (a4.w != 1.0f);
-                    }
-                    resc[hh] = ch;
-                }
+                const uint4 f = *reinterpret_cast<const uint4*>(flag_s + (tau & 1) * 4);
+                resc[0] = (f.x | f.y) != 0u;
+                resc[1] = (f.z | f.w) != 0u;
             }
 
             // P' = 2^(x - m + kPBias) as two E4M3 terms, 16 tokens per 16-byte row.
