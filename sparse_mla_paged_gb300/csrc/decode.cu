@@ -575,27 +575,39 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
         // contiguous bytes.
         const uint4* src = reinterpret_cast<const uint4*>(p.qimg + static_cast<int64_t>(unit) * kQImageBytes +
                                                           half * 16 * 2048 + (q4 * 32 + lane) * 16);
+        // All sixteen loads are issued before either store: one memory round trip.
+        uint32_t a[2][32];
 #pragma unroll
-        for (int hc = 0; hc < 2; ++hc) {
-            uint32_t a[32];
+        for (int hc = 0; hc < 2; ++hc)
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 const uint4 v = src[(hc * 8 + c) * (2048 / 16)];
-                a[4 * c] = v.x;
-                a[4 * c + 1] = v.y;
-                a[4 * c + 2] = v.z;
-                a[4 * c + 3] = v.w;
+                a[hc][4 * c] = v.x;
+                a[hc][4 * c + 1] = v.y;
+                a[hc][4 * c + 2] = v.z;
+                a[hc][4 * c + 3] = v.w;
             }
-            tmem_st_x32(tmem + lane_base + kTmemQ + half * 64 + hc * 32, a);
-        }
+#pragma unroll
+        for (int hc = 0; hc < 2; ++hc) tmem_st_x32(tmem + lane_base + kTmemQ + half * 64 + hc * 32, a[hc]);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(barp(BAR_QFULL));
     };
+    // The next unit's row count and query scale are read at the start of the current one
+    // (plain loads whose latency the unit's tiles hide).
+    Segment s_next = seg0;
+    Tiles tl_next = segment_tokens(p, seg0);
+    float c_next = p.qscale[static_cast<int64_t>(seg0.unit) * kHeadsPerCta + hq];
     for (int i = 0; i < nseg; ++i) {
-        const Segment s = i == 0 ? seg0 : cta_segment(p.part, blockIdx.x, i);
-        const Tiles tl = segment_tokens(p, s);
+        const Segment s = s_next;
+        const Tiles tl = tl_next;
+        const float c = c_next;
+        if (i + 1 < nseg) {
+            s_next = cta_segment(p.part, blockIdx.x, i + 1);
+            tl_next = segment_tokens(p, s_next);
+            c_next = p.qscale[static_cast<int64_t>(s_next.unit) * kHeadsPerCta + hq];
+        }
         const int hvalid = min(kHeadsPerCta, p.heads - s.group * kHeadsPerCta);
         const int64_t head0 = static_cast<int64_t>(s.row) * p.heads + s.group * kHeadsPerCta;
         if (tl.n <= 0) {
@@ -613,7 +625,6 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
         // Query operand of this unit into TMEM, once the previous unit's QKs are done.
         if (qseg > 0) warp_wait(p, barp(BAR_QEMPTY), (qseg - 1) & 1, abort_flag);
         load_q(s.unit);
-        const float c = p.qscale[static_cast<int64_t>(s.unit) * kHeadsPerCta + hq];
         float m_ref = kNegInf;  // reference max of head hq (log2 units)
         float m_top = kNegInf;  // highest reference of head hq so far
         float l_part = 0.0f;    // this thread's share of the row sum of P'
