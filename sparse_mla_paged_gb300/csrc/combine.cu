@@ -1,11 +1,12 @@
 // Log-sum-exp combine of per-CTA partials for work units split across CTAs.
 //
 // A partial k of unit (row, head group) holds O_k = (sum_j 2^(x_j - m_k) V_j) / l_k in
-// E4M3 code units (stored as f16) and lse_k = m_k + log2(l_k), x being the score in log2 units. The
-// softmax over the union of the pieces is out = v_scale * sum_k 2^(lse_k - LSE) O_k with
-// LSE = log2 sum_k 2^lse_k; a piece with no tokens has lse = -inf and weight 0, and a
-// unit whose pieces are all empty is 0. Units owned by one CTA were written directly by
-// the decode kernel and are skipped here.
+// E4M3 code units, stored as f16 laid out [16 blocks of 32 dims][8 head groups][32 dims]
+// [8 heads] (a block's 64 heads x 32 dims are 4 contiguous KB), and
+// lse_k = m_k + log2(l_k), x being the score in log2 units. The softmax over the union of
+// the pieces is out = v_scale * sum_k 2^(lse_k - LSE) O_k with LSE = log2 sum_k 2^lse_k; a
+// piece with no tokens has lse = -inf and weight 0, and a unit whose pieces are all empty
+// is 0. Units owned by one CTA were written directly by the decode kernel and are skipped.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -15,9 +16,11 @@ namespace dsa {
 namespace {
 
 constexpr int kCombineThreads = 256;
-constexpr int kCombineHeads = kCombineThreads / 64;  // heads per block; 64 threads x 8 dims per head
-constexpr int kPieceBatch = 8;                        // partial loads in flight per thread
+constexpr int kCombineWarps = kCombineThreads / 32;  // one per group of 8 heads
+constexpr int kCombineDims = 32;                      // dims per block: the lanes of a warp
+constexpr int kWeightChunk = 16;                      // pieces whose weights sit in shared memory at once
 constexpr float kNegInfC = -__builtin_huge_valf();
+static_assert(kCombineWarps * 8 == kHeadsPerCta, "a warp per 8-head group");
 
 // Partial slot of unit u in CTA c, or -1 when CTA c has no slots at all.
 __device__ __forceinline__ int32_t piece_slot(const Partition& part, int64_t u, int64_t c) {
@@ -26,143 +29,134 @@ __device__ __forceinline__ int32_t piece_slot(const Partition& part, int64_t u, 
     return static_cast<int32_t>(2 * c + (u == b / part.width ? 0 : 1));
 }
 
-// Softmax-weighted sum of a head's pieces; writes v_scale * acc / wsum as BF16.
-__device__ __forceinline__ void store_head(const CombineParams& p, int32_t r, int32_t h, int dim0, const float (&acc)[8],
-                                           float wsum) {
-    if (h >= p.heads) return;
-    const float f = wsum > 0.0f ? p.v_scale / wsum : 0.0f;
-    uint4 packed;
-    uint32_t* pw = reinterpret_cast<uint32_t*>(&packed);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * k] * f, acc[2 * k + 1] * f);
-        pw[k] = *reinterpret_cast<uint32_t*>(&b);
-    }
-    *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(r) * p.heads + h) * kLatent + dim0) = packed;
+// v_scale * 2^(lse - m) / sum for one piece of one head, given f = v_scale / sum (0 for an
+// empty piece, or a head whose pieces are all empty).
+__device__ __forceinline__ float piece_weight(float lse, float m, float f) {
+    return lse != kNegInfC ? f * exp2f(lse - m) : 0.0f;
 }
 
-// Block (u, hb): heads hb*4 .. hb*4+3 of unit u; thread t: head hb*4 + t/64, dims 8*(t%64) ..
-// +8. kFastPieces > 0 (the host's bound on pieces per unit): the pieces' partial slots are
-// found before the grid-dependency wait (they depend on the partition only), then every
-// thread loads its head's lse values and 16-byte slices of all pieces at once and folds
-// them in registers. kFastPieces = 0: the block stages up to 256 pieces' slots and lse
-// values per round in shared memory and folds them into a running softmax, kPieceBatch
-// loads at a time. The variants differ in registers, hence in blocks per SM.
-template <int kFastPieces>
+// Block (u, db): dims 32*db .. 32*db + 31 of unit u, all 64 heads. Warp w takes heads
+// 8w .. 8w + 7 and lane l dim 32*db + l, so the block reads 4 contiguous KB of each partial
+// and each warp load 512 bytes; the output tile is transposed through shared memory. Lanes 0..7 of a warp form the
+// pieces' weights of its 8 heads into the warp's own shared-memory rows (warp-level sync).
+// kFast > 0 (the host's bound on pieces per unit): the pieces' partial slots are found
+// before the grid-dependency wait (they depend on the partition only), then every thread
+// loads its 16-byte slice of every piece at once while the weight lanes load the lse
+// values: one round trip. kFast = 0: any number of pieces, kWeightChunk at a time.
+template <int kFast>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams p) {
     // After a long decode the next call's first kernel may launch now (it waits for this
     // grid to complete); otherwise it launches when this grid exits.
     if (p.early_dependents) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __shared__ int32_t slot_s[kCombineThreads];
-    __shared__ float lse_s[kCombineHeads][kCombineThreads];
+    __shared__ float w_s[kCombineWarps][kWeightChunk][8];
+    __shared__ __align__(16) __nv_bfloat16 out_s[kHeadsPerCta][kCombineDims];  // the block's output tile
     const int64_t u = blockIdx.x;
-    const int hh = threadIdx.x >> 6;
-    const int hl = blockIdx.y * kCombineHeads + hh;
-    const int dim0 = (threadIdx.x & 63) * 8;
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int dim = blockIdx.y * kCombineDims + lane;
     const int32_t r = static_cast<int32_t>(u / p.part.groups), g = static_cast<int32_t>(u % p.part.groups);
-    const int32_t h = g * kHeadsPerCta + hl;
     const int64_t W = p.part.width;
     const int64_t c_lo = cta_of_slot(p.part, u * W);
     const int64_t c_hi = cta_of_slot(p.part, (u + 1) * W - 1);
     const int64_t npieces = c_hi + 1 - c_lo;
     if (npieces == 1) return;  // written whole by the decode kernel (uniform over the block)
+    const __half* po = reinterpret_cast<const __half*>(p.part_o);
+    auto slice = [&](int32_t slot) {  // heads 8*warp .. +8 of this lane's dim in partial `slot`
+        return *reinterpret_cast<const uint4*>(
+            po + static_cast<int64_t>(slot) * kHeadsPerCta * kLatent +
+            ((static_cast<int64_t>(blockIdx.y) * kCombineWarps + warp) * kCombineDims + lane) * 8);
+    };
+    auto lse_of = [&](int32_t slot) {  // lse of head 8*warp + lane (lanes 0..7)
+        return p.part_lse[static_cast<int64_t>(slot) * kHeadsPerCta + warp * 8 + lane];
+    };
+    float acc[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+    auto fold = [&](const uint4& raw, int k) {
+        const __half2* hv = reinterpret_cast<const __half2*>(&raw);
+        const float4 wa = *reinterpret_cast<const float4*>(&w_s[warp][k][0]);
+        const float4 wb = *reinterpret_cast<const float4*>(&w_s[warp][k][4]);
+        const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __half22float2(hv[e]);
+            acc[2 * e] += w[2 * e] * f.x;
+            acc[2 * e + 1] += w[2 * e + 1] * f.y;
+        }
+    };
 
-    if (kFastPieces > 0 && npieces <= kFastPieces) {
-        if (static_cast<int64_t>(threadIdx.x) < npieces) slot_s[threadIdx.x] = piece_slot(p.part, u, c_lo + threadIdx.x);
+    if (kFast > 0 && npieces <= kFast) {
+        const int n = static_cast<int>(npieces);
+        if (t < n) slot_s[t] = piece_slot(p.part, u, c_lo + t);
         __syncthreads();
         // Launched as a programmatic dependent of the decode kernel: wait for its partials.
         asm volatile("griddepcontrol.wait;" ::: "memory");
-        const int n = static_cast<int>(npieces);
-        constexpr int kN = kFastPieces > 0 ? kFastPieces : 1;
-        float lse[kN];
+        constexpr int kN = kFast > 0 ? kFast : 1;
         uint4 raw[kN];
 #pragma unroll
-        for (int e = 0; e < kN; ++e) {
-            lse[e] = kNegInfC;
-            raw[e] = make_uint4(0, 0, 0, 0);
-            if (e < n && slot_s[e] >= 0) {  // a CTA without slots has no piece
-                const int64_t slot = slot_s[e];
-                lse[e] = p.part_lse[slot * kHeadsPerCta + hl];
-                raw[e] = *reinterpret_cast<const uint4*>(p.part_o + (slot * kHeadsPerCta + hl) * kLatent + dim0);
-            }
+        for (int k = 0; k < kN; ++k) {
+            raw[k] = make_uint4(0, 0, 0, 0);
+            if (k < n && slot_s[k] >= 0) raw[k] = slice(slot_s[k]);  // a CTA without slots has no piece
         }
-        float m = kNegInfC;
+        if (lane < 8) {
+            float lse[kN];
+            float m = kNegInfC;
 #pragma unroll
-        for (int e = 0; e < kN; ++e) m = fmaxf(m, lse[e]);
-        float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        float wsum = 0.0f;
-        if (m != kNegInfC) {
+            for (int k = 0; k < kN; ++k) {
+                lse[k] = (k < n && slot_s[k] >= 0) ? lse_of(slot_s[k]) : kNegInfC;
+                m = fmaxf(m, lse[k]);
+            }
+            float sum = 0.0f;
+            if (m != kNegInfC) {
 #pragma unroll
-            for (int e = 0; e < kN; ++e) {
-                const float w = exp2f(lse[e] - m);  // 0 for an empty piece (lse = -inf)
-                wsum += w;
-                const __half2* hv = reinterpret_cast<const __half2*>(&raw[e]);
+                for (int k = 0; k < kN; ++k) sum += exp2f(lse[k] - m);  // 0 for an empty piece
+            }
+            const float f = sum > 0.0f ? p.v_scale / sum : 0.0f;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float2 f = __half22float2(hv[k]);
-                    acc[2 * k] += w * f.x;
-                    acc[2 * k + 1] += w * f.y;
+            for (int k = 0; k < kN; ++k)
+                if (k < n) w_s[warp][k][lane] = piece_weight(lse[k], m, f);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < kN; ++k)
+            if (k < n) fold(raw[k], k);
+    } else {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        // Maximum and sum over every piece, per head (lanes 0..7 of each warp).
+        float m = kNegInfC, sum = 0.0f;
+        if (lane < 8) {
+            for (int64_t k = 0; k < npieces; ++k) {
+                const int32_t slot = piece_slot(p.part, u, c_lo + k);
+                if (slot >= 0) m = fmaxf(m, lse_of(slot));
+            }
+            if (m != kNegInfC)
+                for (int64_t k = 0; k < npieces; ++k) {
+                    const int32_t slot = piece_slot(p.part, u, c_lo + k);
+                    if (slot >= 0) sum += exp2f(lse_of(slot) - m);
                 }
-            }
         }
-        store_head(p, r, h, dim0, acc, wsum);
-        return;
-    }
-
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    float mx = kNegInfC, wsum = 0.0f;
-    float acc[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) acc[k] = 0.0f;
-    for (int64_t c0 = c_lo; c0 <= c_hi; c0 += kCombineThreads) {
-        const int n = static_cast<int>(min(c_hi + 1 - c0, static_cast<int64_t>(kCombineThreads)));
-        __syncthreads();  // the previous round's smem is no longer read
-        if (static_cast<int>(threadIdx.x) < n) {
-            const int32_t slot = piece_slot(p.part, u, c0 + threadIdx.x);
-            slot_s[threadIdx.x] = slot;
-#pragma unroll
-            for (int k = 0; k < kCombineHeads; ++k)
-                lse_s[k][threadIdx.x] =
-                    slot >= 0 ? p.part_lse[static_cast<int64_t>(slot) * kHeadsPerCta + blockIdx.y * kCombineHeads + k]
-                              : kNegInfC;
-        }
-        __syncthreads();
-        float m = mx;
-        for (int e = 0; e < n; ++e) m = fmaxf(m, lse_s[hh][e]);
-        if (m == kNegInfC) continue;
-        if (m > mx) {  // rescale what was folded so far
-            const float a = mx == kNegInfC ? 0.0f : exp2f(mx - m);
-            wsum *= a;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) acc[k] *= a;
-            mx = m;
-        }
-        for (int e0 = 0; e0 < n; e0 += kPieceBatch) {
-            uint4 raw[kPieceBatch];
-            float w[kPieceBatch];
-#pragma unroll
-            for (int e = 0; e < kPieceBatch; ++e) {
-                const int k = e0 + e;
-                w[e] = k < n ? exp2f(lse_s[hh][k] - mx) : 0.0f;
-                raw[e] = make_uint4(0, 0, 0, 0);
-                if (w[e] != 0.0f)
-                    raw[e] = *reinterpret_cast<const uint4*>(
-                        p.part_o + (static_cast<int64_t>(slot_s[k]) * kHeadsPerCta + hl) * kLatent + dim0);
-            }
-#pragma unroll
-            for (int e = 0; e < kPieceBatch; ++e) {
-                wsum += w[e];
-                const __half2* hv = reinterpret_cast<const __half2*>(&raw[e]);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float2 f = __half22float2(hv[k]);
-                    acc[2 * k] += w[e] * f.x;
-                    acc[2 * k + 1] += w[e] * f.y;
-                }
-            }
+        const float f = sum > 0.0f ? p.v_scale / sum : 0.0f;
+        for (int64_t k0 = 0; k0 < npieces; k0 += kWeightChunk) {
+            const int n = static_cast<int>(min(npieces - k0, static_cast<int64_t>(kWeightChunk)));
+            __syncthreads();  // the previous chunk's slots and weights are no longer read
+            if (t < n) slot_s[t] = piece_slot(p.part, u, c_lo + k0 + t);
+            __syncthreads();
+            if (lane < 8)
+                for (int k = 0; k < n; ++k)
+                    w_s[warp][k][lane] = slot_s[k] >= 0 ? piece_weight(lse_of(slot_s[k]), m, f) : 0.0f;
+            __syncwarp();
+            for (int k = 0; k < n; ++k)
+                if (slot_s[k] >= 0) fold(slice(slot_s[k]), k);
         }
     }
-    store_head(p, r, h, dim0, acc, wsum);
+    // The block's output tile [64 heads][32 dims] goes through shared memory, so that each
+    // thread writes 16 bytes (8 dims of one head) of the BF16 output rows.
+#pragma unroll
+    for (int e = 0; e < 8; ++e) out_s[warp * 8 + e][lane] = __float2bfloat16_rn(acc[e]);
+    __syncthreads();
+    const int hl = t / 4, c = (t % 4) * 8;
+    if (hl < p.heads - g * kHeadsPerCta)
+        *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
+                                  (static_cast<int64_t>(r) * p.heads + g * kHeadsPerCta + hl) * kLatent +
+                                  blockIdx.y * kCombineDims + c) = *reinterpret_cast<const uint4*>(&out_s[hl][c]);
 }
 
 }  // namespace
@@ -184,7 +178,7 @@ cudaError_t combine_kernel_setup() {
 cudaError_t launch_combine(const CombineParams& p, int units, int max_pieces, cudaStream_t stream) {
     if (units <= 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(units, kHeadsPerCta / kCombineHeads);
+    cfg.gridDim = dim3(units, kLatent / kCombineDims);
     cfg.blockDim = dim3(kCombineThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;

@@ -788,25 +788,40 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
             uint32_t v64[64];
             tmem_ld_x64(tmem + lane_base + kTmemO + mc * 64, v64);
             if (st == 0 && i == 0 && mc2 == 0) DSA_TRACE_AT(p, 14);
+            if (whole) {
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                float o[32], f[32];
+                for (int hh = 0; hh < 2; ++hh) {
+                    float o[32], f[32];
 #pragma unroll
-                for (int k = 0; k < 32; k += 4) {
-                    const float4 f4 = *reinterpret_cast<const float4*>(f_s + hh * 32 + k);
-                    f[k] = f4.x;
-                    f[k + 1] = f4.y;
-                    f[k + 2] = f4.z;
-                    f[k + 3] = f4.w;
-                }
+                    for (int k = 0; k < 32; k += 4) {
+                        const float4 f4 = *reinterpret_cast<const float4*>(f_s + hh * 32 + k);
+                        f[k] = f4.x;
+                        f[k + 1] = f4.y;
+                        f[k + 2] = f4.z;
+                        f[k + 3] = f4.w;
+                    }
 #pragma unroll
-                for (int k = 0; k < 32; ++k) o[k] = __uint_as_float(v64[hh * 32 + k]);
-                if (whole) {
+                    for (int k = 0; k < 32; ++k) o[k] = __uint_as_float(v64[hh * 32 + k]);
                     __nv_bfloat16* rows = reinterpret_cast<__nv_bfloat16*>(p.out) + head0 * kLatent;
                     store_block(rows, hh * 32, hvalid, dim0, o, f, stage, lane);
-                } else {
-                    __half* rows = reinterpret_cast<__half*>(p.part_o) + static_cast<int64_t>(s.part) * kHeadsPerCta * kLatent;
-                    store_block(rows, hh * 32, kHeadsPerCta, dim0, o, f, stage, lane);
+                }
+            } else {
+                // A partial is [16 blocks of 32 dims][8 head groups][32 dims][8 heads] f16:
+                // this lane's dim holds all 64 heads, and each store instruction of the warp
+                // writes one head group of its 32 dims, 512 contiguous bytes, straight from
+                // registers (dim0 is a multiple of 32: the warp's dims are one dim block).
+                __half* part = reinterpret_cast<__half*>(p.part_o) + static_cast<int64_t>(s.part) * kHeadsPerCta * kLatent;
+#pragma unroll
+                for (int k = 0; k < kHeadsPerCta; k += 8) {
+                    const float4 fa = *reinterpret_cast<const float4*>(f_s + k);
+                    const float4 fb = *reinterpret_cast<const float4*>(f_s + k + 4);
+                    const __half2 h0 = __floats2half2_rn(__uint_as_float(v64[k]) * fa.x, __uint_as_float(v64[k + 1]) * fa.y);
+                    const __half2 h1 = __floats2half2_rn(__uint_as_float(v64[k + 2]) * fa.z, __uint_as_float(v64[k + 3]) * fa.w);
+                    const __half2 h2 = __floats2half2_rn(__uint_as_float(v64[k + 4]) * fb.x, __uint_as_float(v64[k + 5]) * fb.y);
+                    const __half2 h3 = __floats2half2_rn(__uint_as_float(v64[k + 6]) * fb.z, __uint_as_float(v64[k + 7]) * fb.w);
+                    *reinterpret_cast<uint4*>(part + ((static_cast<int64_t>(dim0 / 32) * 8 + k / 8) * 32 + lane) * 8) =
+                        make_uint4(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1),
+                                   *reinterpret_cast<const uint32_t*>(&h2), *reinterpret_cast<const uint32_t*>(&h3));
                 }
             }
         }
