@@ -460,9 +460,11 @@ __device__ void run_mma(const DecodeParams& p, uint32_t sbase, uint32_t tmem, vo
     };
 
     uint32_t tau = 0;
+    Tiles tl_next = segment_tokens(p, seg0);
     for (int i = 0; i < nseg; ++i) {
-        const Segment s = i == 0 ? seg0 : cta_segment(p.part, blockIdx.x, i);
-        const Tiles tl = segment_tokens(p, s);
+        const Tiles tl = tl_next;
+        // The next unit's count is read a unit ahead, its latency hidden behind this unit.
+        if (i + 1 < nseg) tl_next = segment_tokens(p, cta_segment(p.part, blockIdx.x, i + 1));
         if (tl.n <= 0) continue;
         mma_wait(p, barp(BAR_QFULL), qseg & 1, abort_flag);
         tc_fence_after();
@@ -630,6 +632,11 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
         float l_part = 0.0f;    // this thread's share of the row sum of P'
 
         for (int t = 0; t < tl.ntiles; ++t, ++tau) {
+            // The next unit's query image was written by the prologue long before and has
+            // left L2 under the gather stream: fetch it back a few tiles before it is read.
+            if (st < 16 && i + 1 < nseg && tl_next.n > 0 && t == max(0, tl.ntiles - 3))
+                bulk_prefetch_l2(p.qimg + static_cast<int64_t>(s_next.unit) * kQImageBytes + st * (kQImageBytes / 16),
+                                 kQImageBytes / 16);
             const int sb = static_cast<int>(tau % kSBufs);
             warp_wait(p, barp(BAR_SFULL0 + sb), (tau / kSBufs) & 1, abort_flag);
             if (st == 0 && tau < 8) DSA_TRACE_AT(p, 24 + tau);
