@@ -600,6 +600,7 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
     // (plain loads whose latency the unit's tiles hide).
     Segment s_next = seg0;
     Tiles tl_next = segment_tokens(p, seg0);
+    bool q_loaded = false;  // the current unit's query operand was loaded during the previous unit
     float c_next = p.qscale[static_cast<int64_t>(seg0.unit) * kHeadsPerCta + hq];
     for (int i = 0; i < nseg; ++i) {
         const Segment s = s_next;
@@ -624,9 +625,13 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
             }
             continue;
         }
-        // Query operand of this unit into TMEM, once the previous unit's QKs are done.
-        if (qseg > 0) warp_wait(p, barp(BAR_QEMPTY), (qseg - 1) & 1, abort_flag);
-        load_q(s.unit);
+        // Query operand of this unit into TMEM, once the previous unit's QKs are done
+        // (already there when it was loaded before the previous unit's epilogue).
+        if (!q_loaded) {
+            if (qseg > 0) warp_wait(p, barp(BAR_QEMPTY), (qseg - 1) & 1, abort_flag);
+            load_q(s.unit);
+        }
+        q_loaded = false;
         float m_ref = kNegInf;  // reference max of head hq (log2 units)
         float m_top = kNegInf;  // highest reference of head hq so far
         float l_part = 0.0f;    // this thread's share of the row sum of P'
@@ -769,6 +774,15 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
             __syncwarp();
             if (lane == 0) mbar_arrive(barp(BAR_PFULL0 + (tau & 1)));
             if (st == 0 && tau < 8) DSA_TRACE_AT(p, 32 + tau);
+        }
+
+        // The next unit's query operand goes into TMEM now, while this unit's last P.V
+        // runs (this unit's last QK completed QEMPTY phase qseg), so that the next unit's
+        // first QK runs during the epilogue below.
+        if (i + 1 < nseg && tl_next.n > 0) {
+            warp_wait(p, barp(BAR_QEMPTY), qseg & 1, abort_flag);
+            load_q(s_next.unit);
+            q_loaded = true;
         }
 
         // ---- epilogue ----
