@@ -161,6 +161,7 @@ Plan make_plan(int64_t rows, int32_t heads, int32_t width, int32_t num_ctas, int
         if (c < 1) c = 1;
     }
     pl.part.ctas = static_cast<int32_t>(c);
+    pl.part.narrow = pl.part.total_slots * (c + 1) < (int64_t{1} << 32) ? 1 : 0;
     pl.small_tiles = tile_tokens == 0 ? pl.part.total_slots <= 2 * kCtaMinSlots * c : tile_tokens == 64;
     pl.any_split = false;
     for (int64_t k = 1; k < c && !pl.any_split; ++k)

@@ -22,11 +22,29 @@ constexpr int kWeightChunk = 16;                      // pieces whose weights si
 constexpr float kNegInfC = -__builtin_huge_valf();
 static_assert(kCombineWarps * 8 == kHeadsPerCta, "a warp per 8-head group");
 
+// The partition's arithmetic (cta_begin, cta_of_slot of common.cuh), in 32-bit unsigned
+// arithmetic when every product fits (exact either way; a 64-bit division is a long
+// software sequence, and each block of this kernel does several before its first load).
+template <bool kNarrow>
+__device__ __forceinline__ int64_t div_c(int64_t a, int64_t b) {
+    if constexpr (kNarrow) return static_cast<int64_t>(static_cast<uint32_t>(a) / static_cast<uint32_t>(b));
+    else return a / b;
+}
+template <bool kNarrow>
+__device__ __forceinline__ int64_t begin_c(const Partition& part, int64_t c) {
+    return div_c<kNarrow>(c * part.total_slots, part.ctas);
+}
+template <bool kNarrow>
+__device__ __forceinline__ int64_t cta_of_c(const Partition& part, int64_t x) {
+    return div_c<kNarrow>((x + 1) * part.ctas - 1, part.total_slots);
+}
+
 // Partial slot of unit u in CTA c, or -1 when CTA c has no slots at all.
+template <bool kNarrow>
 __device__ __forceinline__ int32_t piece_slot(const Partition& part, int64_t u, int64_t c) {
-    const int64_t b = cta_begin(part, c);
-    if (b >= cta_begin(part, c + 1)) return -1;
-    return static_cast<int32_t>(2 * c + (u == b / part.width ? 0 : 1));
+    const int64_t b = begin_c<kNarrow>(part, c);
+    if (b >= begin_c<kNarrow>(part, c + 1)) return -1;
+    return static_cast<int32_t>(2 * c + (u == div_c<kNarrow>(b, part.width) ? 0 : 1));
 }
 
 // v_scale * 2^(lse - m) / sum for one piece of one head, given f = v_scale / sum (0 for an
@@ -43,7 +61,7 @@ __device__ __forceinline__ float piece_weight(float lse, float m, float f) {
 // before the grid-dependency wait (they depend on the partition only), then every thread
 // loads its 16-byte slice of every piece at once while the weight lanes load the lse
 // values: one round trip. kFast = 0: any number of pieces, kWeightChunk at a time.
-template <int kFast>
+template <int kFast, bool kNarrow>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams p) {
     // After a long decode the next call's first kernel may launch now (it waits for this
     // grid to complete); otherwise it launches when this grid exits.
@@ -54,10 +72,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
     const int64_t u = blockIdx.x;
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int dim = blockIdx.y * kCombineDims + lane;
-    const int32_t r = static_cast<int32_t>(u / p.part.groups), g = static_cast<int32_t>(u % p.part.groups);
+    const int32_t r = static_cast<int32_t>(div_c<kNarrow>(u, p.part.groups));
+    const int32_t g = static_cast<int32_t>(u - static_cast<int64_t>(r) * p.part.groups);
     const int64_t W = p.part.width;
-    const int64_t c_lo = cta_of_slot(p.part, u * W);
-    const int64_t c_hi = cta_of_slot(p.part, (u + 1) * W - 1);
+    const int64_t c_lo = cta_of_c<kNarrow>(p.part, u * W);
+    const int64_t c_hi = cta_of_c<kNarrow>(p.part, (u + 1) * W - 1);
     const int64_t npieces = c_hi + 1 - c_lo;
     if (npieces == 1) return;  // written whole by the decode kernel (uniform over the block)
     const __half* po = reinterpret_cast<const __half*>(p.part_o);
@@ -85,7 +104,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
 
     if (kFast > 0 && npieces <= kFast) {
         const int n = static_cast<int>(npieces);
-        if (t < n) slot_s[t] = piece_slot(p.part, u, c_lo + t);
+        if (t < n) slot_s[t] = piece_slot<kNarrow>(p.part, u, c_lo + t);
         __syncthreads();
         // Launched as a programmatic dependent of the decode kernel: wait for its partials.
         asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -124,12 +143,12 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
         float m = kNegInfC, sum = 0.0f;
         if (lane < 8) {
             for (int64_t k = 0; k < npieces; ++k) {
-                const int32_t slot = piece_slot(p.part, u, c_lo + k);
+                const int32_t slot = piece_slot<kNarrow>(p.part, u, c_lo + k);
                 if (slot >= 0) m = fmaxf(m, lse_of(slot));
             }
             if (m != kNegInfC)
                 for (int64_t k = 0; k < npieces; ++k) {
-                    const int32_t slot = piece_slot(p.part, u, c_lo + k);
+                    const int32_t slot = piece_slot<kNarrow>(p.part, u, c_lo + k);
                     if (slot >= 0) sum += exp2f(lse_of(slot) - m);
                 }
         }
@@ -137,7 +156,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
         for (int64_t k0 = 0; k0 < npieces; k0 += kWeightChunk) {
             const int n = static_cast<int>(min(npieces - k0, static_cast<int64_t>(kWeightChunk)));
             __syncthreads();  // the previous chunk's slots and weights are no longer read
-            if (t < n) slot_s[t] = piece_slot(p.part, u, c_lo + k0 + t);
+            if (t < n) slot_s[t] = piece_slot<kNarrow>(p.part, u, c_lo + k0 + t);
             __syncthreads();
             if (lane < 8)
                 for (int k = 0; k < n; ++k)
@@ -162,9 +181,12 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
 }  // namespace
 
 cudaError_t combine_kernel_setup() {
-    const void* fns[] = {reinterpret_cast<const void*>(combine_kernel<0>),
-                         reinterpret_cast<const void*>(combine_kernel<4>),
-                         reinterpret_cast<const void*>(combine_kernel<16>)};
+    const void* fns[] = {reinterpret_cast<const void*>(combine_kernel<0, false>),
+                         reinterpret_cast<const void*>(combine_kernel<4, false>),
+                         reinterpret_cast<const void*>(combine_kernel<16, false>),
+                         reinterpret_cast<const void*>(combine_kernel<0, true>),
+                         reinterpret_cast<const void*>(combine_kernel<4, true>),
+                         reinterpret_cast<const void*>(combine_kernel<16, true>)};
     for (const void* f : fns) {
         cudaFuncAttributes attr;
         cudaError_t e = cudaFuncGetAttributes(&attr, f);
@@ -187,9 +209,14 @@ cudaError_t launch_combine(const CombineParams& p, int units, int max_pieces, cu
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (max_pieces <= 4) return cudaLaunchKernelEx(&cfg, combine_kernel<4>, p);
-    if (max_pieces <= 16) return cudaLaunchKernelEx(&cfg, combine_kernel<16>, p);
-    return cudaLaunchKernelEx(&cfg, combine_kernel<0>, p);
+    if (p.part.narrow) {
+        if (max_pieces <= 4) return cudaLaunchKernelEx(&cfg, combine_kernel<4, true>, p);
+        if (max_pieces <= 16) return cudaLaunchKernelEx(&cfg, combine_kernel<16, true>, p);
+        return cudaLaunchKernelEx(&cfg, combine_kernel<0, true>, p);
+    }
+    if (max_pieces <= 4) return cudaLaunchKernelEx(&cfg, combine_kernel<4, false>, p);
+    if (max_pieces <= 16) return cudaLaunchKernelEx(&cfg, combine_kernel<16, false>, p);
+    return cudaLaunchKernelEx(&cfg, combine_kernel<0, false>, p);
 }
 
 }  // namespace dsa

@@ -82,6 +82,7 @@ struct Partition {
     int32_t width;        // W
     int32_t ctas;         // C
     int32_t groups;       // G
+    int32_t narrow;       // T*(C+1) < 2^32: the combine kernel divides in 32 bits
 };
 
 __host__ __device__ inline int64_t cta_begin(const Partition& p, int64_t c) {
