@@ -753,19 +753,22 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
                 // tile's P.V waits for the rescale through the P-full barrier below.
                 warp_wait(p, barp(BAR_PVDONE0 + ((tau - 1) & 1)), ((tau - 1) >> 1) & 1, abort_flag);
                 tc_fence_after();
+                // Both dim chunks of a 32-head block are loaded together (one load latency
+                // per block instead of one per chunk) and share the block's 32 factors.
 #pragma unroll 1
-                for (int mc2 = 0; mc2 < 2; ++mc2) {
-#pragma unroll 1
-                    for (int hh = 0; hh < 2; ++hh) {
-                        if (!resc[hh]) continue;
-                        const uint32_t ta = tmem + lane_base + kTmemO + (2 * half + mc2) * 64 + hh * 32;
-                        uint32_t o[32];
-                        tmem_ld_x32(ta, o);
+                for (int hh = 0; hh < 2; ++hh) {
+                    if (!resc[hh]) continue;
+                    const uint32_t ta = tmem + lane_base + kTmemO + 2 * half * 64 + hh * 32;
+                    uint32_t o0[32], o1[32];
+                    tmem_ld_2x32(ta, ta + 64, o0, o1);
 #pragma unroll
-                        for (int k = 0; k < 32; ++k)
-                            o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha_t[hh * 32 + k]);
-                        tmem_st_x32(ta, o);
+                    for (int k = 0; k < 32; ++k) {
+                        const float f = alpha_t[hh * 32 + k];
+                        o0[k] = __float_as_uint(__uint_as_float(o0[k]) * f);
+                        o1[k] = __float_as_uint(__uint_as_float(o1[k]) * f);
                     }
+                    tmem_st_x32(ta, o0);
+                    tmem_st_x32(ta + 64, o1);
                 }
                 tmem_wait_st();
             }
