@@ -359,9 +359,7 @@ def needs_combine(api, w, ctas) -> bool:
     # The combine runs when some CTA boundary of the slot partition falls inside a unit.
     groups = (w.num_q_heads + 63) // 64
     T = w.rows * groups * w.sel_width
-    if ctas <= 0:
-        sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-        ctas = max(1, min(sms, (T + 127) // 128))
+    ctas = api.decode_grid(w.num_seqs, w.rows_per_seq, w.num_q_heads, w.sel_width, ctas)
     return any((k * T // ctas) % w.sel_width != 0 for k in range(1, ctas))
 
 

@@ -132,12 +132,23 @@ size_t dsa_mla_decode_workspace_bytes(int32_t num_seqs, int32_t rows_per_seq,
                                       int32_t num_q_heads, int32_t sel_width, int32_t num_ctas);
 
 /*
+ * Decode grid size (CTAs) that a call of this shape runs with: num_ctas itself when it
+ * is positive, else the default for the current device (0 if no CUDA device is
+ * available or an argument is out of range). The default takes at most one CTA per SM
+ * and at least 128 slots (selection positions of one 64-head group of one row) per CTA,
+ * and prefers a count aligned with the units (rows x 64-head groups): a multiple of the
+ * unit count or a divisor of it, when one is at least three quarters of that bound.
+ */
+int32_t dsa_mla_decode_grid(int32_t num_seqs, int32_t rows_per_seq, int32_t num_q_heads,
+                            int32_t sel_width, int32_t num_ctas);
+
+/*
  * Per-call options of dsa_mla_decode_ws (NULL = all defaults). Zero-initialise and set the
  * fields you need; zero means "default" in every field. The source pages have no
  * counterpart to these options: they choose between equivalent launch shapes or serve
  * measurement and testing, and never change what is computed beyond floating-point
  * rounding order.
- *  num_ctas       decode grid size; 0 = default (the SM count, fewer for small problems).
+ *  num_ctas       decode grid size; 0 = default (dsa_mla_decode_grid: at most the SM count).
  *                 Must match the num_ctas the workspace was sized for.
  *  tile_tokens    KV tokens per decode tile: 0 = automatic (64-token tiles when each
  *                 decode CTA has at most 256 selected slots of work, 128 otherwise),

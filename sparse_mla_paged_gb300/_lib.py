@@ -42,6 +42,7 @@ SIGNATURES = {
     "dsa_mla_decode_k": (_DECODE_ARGS + [_P], _I32),
     "dsa_mla_decode_static": (_DECODE_ARGS + [_P], _I32),
     "dsa_mla_decode_workspace_bytes": ([_I32, _I32, _I32, _I32, _I32], _SZ),
+    "dsa_mla_decode_grid": ([_I32, _I32, _I32, _I32, _I32], _I32),
     "dsa_mla_decode_ws": (_DECODE_ARGS + [_I32, _P, _SZ, ctypes.POINTER(DecodeOptions), _P], _I32),
     "dsa_mla_decode_host_workspace_bytes": ([_I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32], _SZ),
     "dsa_mla_decode_host": ([_P, _P, _P, _P, _I32, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I64, _F32,

@@ -84,6 +84,12 @@ def workspace_bytes(num_seqs, rows_per_seq, num_q_heads, sel_width, num_ctas=0) 
                                                           int(sel_width), int(num_ctas)))
 
 
+def decode_grid(num_seqs, rows_per_seq, num_q_heads, sel_width, num_ctas=0) -> int:
+    """Decode grid size a call of this shape runs with (dsa_mla_decode_grid; 0 = none)."""
+    return int(_lib.load().dsa_mla_decode_grid(int(num_seqs), int(rows_per_seq), int(num_q_heads),
+                                               int(sel_width), int(num_ctas)))
+
+
 def alloc_workspace(num_seqs, rows_per_seq, num_q_heads, sel_width, num_ctas=0, device=None) -> torch.Tensor:
     n = workspace_bytes(num_seqs, rows_per_seq, num_q_heads, sel_width, num_ctas)
     if n == 0:

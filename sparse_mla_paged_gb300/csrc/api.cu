@@ -146,6 +146,23 @@ int32_t read_options(const dsa_decode_options* o, CallOptions* out) {
     return DSA_OK;
 }
 
+// Default decode grid. At most one CTA per SM and at least kCtaMinSlots slots per CTA
+// (c_max); within that, a grid aligned with the units is preferred: a CTA count that is a
+// multiple of the unit count (every CTA's slots lie in one unit, each unit split into
+// equal pieces) or divides it (every CTA takes whole units). Such a grid has no CTA that
+// changes unit in mid-range and no unit that ends inside a CTA, which saves a unit change
+// per CTA and, when each CTA takes whole units, the combine; measured on GB300 it beats an
+// unaligned grid with up to a third more CTAs. The largest aligned count is taken when it
+// is at least three quarters of c_max, else c_max.
+int64_t default_grid(int64_t units, int64_t total_slots, int sms) {
+    int64_t c_max = (total_slots + kCtaMinSlots - 1) / kCtaMinSlots;
+    if (c_max > sms) c_max = sms;
+    if (c_max < 1) c_max = 1;
+    for (int64_t c = c_max; 4 * c >= 3 * c_max; --c)
+        if (c % units == 0 || units % c == 0) return c;
+    return c_max;
+}
+
 Plan make_plan(int64_t rows, int32_t heads, int32_t width, int32_t num_ctas, int sms, int32_t tile_tokens = 0) {
     Plan pl;
     pl.rows = rows;
@@ -155,11 +172,7 @@ Plan make_plan(int64_t rows, int32_t heads, int32_t width, int32_t num_ctas, int
     pl.part.width = width;
     pl.part.groups = static_cast<int32_t>(pl.groups);
     int64_t c = num_ctas;
-    if (c <= 0) {
-        c = (pl.part.total_slots + kCtaMinSlots - 1) / kCtaMinSlots;
-        if (c > sms) c = sms;
-        if (c < 1) c = 1;
-    }
+    if (c <= 0) c = default_grid(pl.units, pl.part.total_slots, sms);
     pl.part.ctas = static_cast<int32_t>(c);
     pl.part.narrow = pl.part.total_slots * (c + 1) < (int64_t{1} << 32) ? 1 : 0;
     pl.small_tiles = tile_tokens == 0 ? pl.part.total_slots <= 2 * kCtaMinSlots * c : tile_tokens == 64;
@@ -426,6 +439,18 @@ size_t dsa_mla_decode_workspace_bytes(int32_t num_seqs, int32_t rows_per_seq, in
         sms = d->sms;
     }
     return make_plan(static_cast<int64_t>(num_seqs) * rows_per_seq, num_q_heads, sel_width, num_ctas, sms).ws.total;
+}
+
+int32_t dsa_mla_decode_grid(int32_t num_seqs, int32_t rows_per_seq, int32_t num_q_heads, int32_t sel_width,
+                            int32_t num_ctas) {
+    if (num_seqs < 1 || rows_per_seq < 1 || num_q_heads < 1 || sel_width < 1 || num_ctas < 0) return 0;
+    int sms = 0;
+    if (num_ctas == 0) {
+        DeviceState* d = nullptr;
+        if (current_device(&d) != DSA_OK) return 0;
+        sms = d->sms;
+    }
+    return make_plan(static_cast<int64_t>(num_seqs) * rows_per_seq, num_q_heads, sel_width, num_ctas, sms).part.ctas;
 }
 
 int32_t dsa_mla_decode_ws(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,

@@ -25,7 +25,7 @@ def _declared_functions():
 def test_header_declares_expected_entry_points():
     names = _declared_functions()
     for want in ("dsa_mla_decode", "dsa_mla_decode_k", "dsa_mla_decode_ws", "dsa_resolve_indices",
-                 "dsa_mla_decode_workspace_bytes", "dsa_status_string", "dsa_read_device_status",
+                 "dsa_mla_decode_workspace_bytes", "dsa_mla_decode_grid", "dsa_status_string", "dsa_read_device_status",
                  "dsa_mla_decode_host", "dsa_latent_write", "dsa_select_pools", "dsa_absorb_q", "dsa_absorb_o"):
         assert want in names
 
@@ -120,6 +120,13 @@ def test_workspace_size_grows_with_the_problem(lib):
     assert base >= rows * width * (4 + 8) + rows * 4 + rows * 65536 + 2 * ctas * 64 * 512 * 2
     assert f(0, 1, 64, 2048, 152) == 0
 
+
+
+def test_explicit_grid_is_taken_as_given(lib):
+    f = lib.dsa_mla_decode_grid
+    assert f(128, 1, 128, 2048, 152) == 152
+    assert f(1, 1, 4, 64, 7) == 7
+    assert f(0, 1, 64, 2048, 152) == 0 and f(8, 1, 64, 2048, -1) == 0 and f(8, 1, 0, 2048, 1) == 0
 
 
 def test_latent_write_rejects_bad_arguments_on_host(lib):

@@ -125,6 +125,41 @@ def test_decode_cta_counts(api, ctas):
     assert api.read_device_status(ws) == 0
 
 
+def _aligned_default(units, slots, sms):
+    c_max = max(1, min(sms, -(-slots // 128)))
+    for c in range(c_max, 0, -1):
+        if 4 * c < 3 * c_max:
+            break
+        if c % units == 0 or units % c == 0:
+            return c
+    return c_max
+
+
+@pytest.mark.parametrize("seqs,k,heads,width", [(128, 1, 128, 2048), (64, 1, 64, 2048), (32, 4, 64, 2048),
+                                                 (8, 1, 64, 2048), (80, 1, 64, 2048), (1, 1, 4, 64),
+                                                 (3, 1, 64, 300)])
+def test_default_grid_prefers_unit_alignment(api, seqs, k, heads, width):
+    """The default grid: at most one CTA per SM and 128 slots per CTA, and the largest
+    count that is a multiple or a divisor of the unit count when it is at least 3/4 of
+    that bound (no CTA then changes unit in mid-range)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    units = seqs * k * ((heads + 63) // 64)
+    got = api.decode_grid(seqs, k, heads, width)
+    assert got == _aligned_default(units, units * width, sms)
+    if sms == 152 and (seqs, k, heads) in ((128, 1, 128), (64, 1, 64), (32, 4, 64), (8, 1, 64)):
+        assert got == 128                    # the four large workloads' shapes on GB300
+    assert api.decode_grid(seqs, k, heads, width, 5) == 5
+
+
+def test_default_grid_decodes_whole_units_without_combine(api):
+    """Eight rows of 64 heads on 4 CTAs (two whole units each): parity, and every CTA
+    boundary on a unit boundary."""
+    w = wl.random_case(num_seqs=8, heads=64, seq_len=900, sel_width=256, seed=21)
+    ws = api.alloc_workspace(8, 1, 64, 256, num_ctas=4)
+    _check(api, w, "4 CTAs over 8 units", workspace=ws, num_ctas=4, status_ok=False)
+    assert api.read_device_status(ws) == 0
+
+
 @pytest.mark.parametrize("width,ctas", [(10, 15), (64, 100)])
 def test_more_ctas_than_slots(api, width, ctas):
     """CTAs without slots leave no piece; the combine skips them."""
