@@ -4,14 +4,14 @@
 // unit = (decode row, group of 64 query heads). Tiles of 128 resolved tokens stream
 // through a 3-tile shared-memory ring (1 tile when K and V are separate buffers):
 //
-//   gather   warps 0-2   cp.async 16-byte copies of each token's 512-byte E4M3 latent row,
-//                        each warp a third of every tile (byte offsets resolved by the
+//   gather   warps 0-3   cp.async 16-byte copies of each token's 512-byte E4M3 latent row,
+//                        each warp a quarter of every tile (byte offsets resolved by the
 //                        prologue; the next tile's offsets are loaded while waiting for a
 //                        free slot), written in the 128-byte-swizzled operand layout, 8
 //                        tokens (4 KB) per swizzle group.
-//   QK^T     warp 3      tcgen05.mma kind::f8f6f4, M = 128 query rows (64 heads x {hi, lo}
+//   QK^T     warp 4      tcgen05.mma kind::f8f6f4, M = 128 query rows (64 heads x {hi, lo}
 //                        terms, A in tensor memory), N = 128 tokens, K = 512: S -> TMEM.
-//   softmax  warps 4-11  the hi and lo rows of a head sit in neighbouring TMEM lanes, so
+//   softmax  warps 5-12  the hi and lo rows of a head sit in neighbouring TMEM lanes, so
 //                        one shuffle gives each thread the full scores of one head for 32
 //                        tokens. A head's reference max is raised only when a tile exceeds
 //                        it by more than kRescaleMargin (one barrier-reduction per tile
@@ -54,11 +54,14 @@ namespace DSA_CAT(tile, DSA_TILE) {
 constexpr int kTileTokens = DSA_TILE;                     // tokens per decode tile = MMA N of QK
 constexpr int kKvTileBytes = kTileTokens * kLatent;       // E4M3 bytes per tile
 
-constexpr int kProducerWarps = 3;
-constexpr int kMmaWarp = 3;
-constexpr int kSoftmaxWarp0 = 4;
+constexpr int kProducerWarps = 4;
+constexpr int kMmaWarp = 4;
+constexpr int kSoftmaxWarp0 = 5;
 constexpr int kSoftmaxWarps = 8;
-constexpr int kThreads = (kSoftmaxWarp0 + kSoftmaxWarps) * 32;  // 384: 3 warps per SM sub-partition
+// 416 threads: one gather warp per SM sub-partition (their copies are issue-bound per
+// warp, and a fourth warp measured faster than three on every large workload) and two
+// softmax warps each; thirteen warps leave 128 registers per thread.
+constexpr int kThreads = (kSoftmaxWarp0 + kSoftmaxWarps) * 32;
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
 
 constexpr int kBarSoftmax = 1;  // named barrier over the softmax warps
@@ -184,7 +187,7 @@ struct Ring {
 // ------------------------------------------------------------------------------------
 // gather warps
 // ------------------------------------------------------------------------------------
-// Rows of a tile taken by gather warp w: [w*43, min(w*43 + 43, 128)).
+// Rows of a tile taken by gather warp w: [w*kWarpRows, min((w+1)*kWarpRows, kTileTokens)).
 constexpr int kWarpRows = (kTileTokens + kProducerWarps - 1) / kProducerWarps;
 
 __device__ void run_producer(const DecodeParams& p, uint32_t sbase, volatile int* abort_flag, int nseg,
@@ -862,7 +865,7 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
     if (st == 0) DSA_TRACE_AT(p, 19);
 }
 
-// kTma: gather by tensor map (warp 0) or by per-thread copies (warps 0-2). The two are
+// kTma: gather by tensor map (warp 0) or by per-thread copies (warps 0-3). The two are
 // separate kernels so that each carries only its own gather code (the warps of one CTA
 // run different code at once and share the SM's instruction cache) and the per-thread
 // copy kernel takes no tensor maps.
