@@ -80,7 +80,8 @@ __device__ void resolve_row(const PrologueParams& p, int32_t r, uint32_t* sm, in
     }
     if (L <= kBitmapWords * 32) {
         const int32_t nwords = (L + 31) >> 5;
-        for (int32_t w = tid; w < nwords; w += kResolveThreads) sm[w] = 0u;
+        uint4* sm4 = reinterpret_cast<uint4*>(sm);
+        for (int32_t w = tid; w < (nwords + 3) >> 2; w += kResolveThreads) sm4[w] = make_uint4(0u, 0u, 0u, 0u);
         __syncthreads();
         for (int32_t j0 = tid;; j0 += kBatch * kResolveThreads) {
 #pragma unroll
@@ -97,19 +98,37 @@ __device__ void resolve_row(const PrologueParams& p, int32_t r, uint32_t* sm, in
             }
         }
         __syncthreads();
-        const int32_t per = (nwords + kResolveThreads - 1) / kResolveThreads;
-        const int32_t w0 = tid * per;
-        const int32_t w1 = min(w0 + per, nwords);
+        // Each warp takes a contiguous range of words (a multiple of 32) and reads it 32
+        // consecutive words at a time (one word per lane, free of bank conflicts): a count
+        // pass, a block scan of the warp totals, then an extraction pass in which a warp
+        // scan of the words' bit counts places every lane's ids.
+        const int lane = tid & 31, warp = tid >> 5;
+        const int32_t wpw = ((nwords + kResolveThreads - 1) / kResolveThreads) * 32;
+        const int32_t wbeg = warp * wpw;
+        const int32_t wend = min(wbeg + wpw, nwords);
         int32_t mine = 0;
-        for (int32_t w = w0; w < w1; ++w) mine += __popc(sm[w]);
-        int32_t pos = block_exclusive_scan(mine, scratch, &total);
-        for (int32_t w = w0; w < w1; ++w) {
-            uint32_t bits = sm[w];
+        for (int32_t w = wbeg + lane; w < wend; w += 32) mine += __popc(sm[w]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+        int32_t pos = block_exclusive_scan(lane == 0 ? mine : 0, scratch, &total);
+        pos = __shfl_sync(0xffffffffu, pos, 0);
+        for (int32_t w0 = wbeg; w0 < wend; w0 += 32) {
+            const int32_t w = w0 + lane;
+            uint32_t bits = w < wend ? sm[w] : 0u;
+            const int32_t c = __popc(bits);
+            int32_t incl = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            int32_t at = pos + incl - c;
             while (bits) {
                 const int b = __ffs(bits) - 1;
-                ids_s[pos++] = w * 32 + b;
+                ids_s[at++] = w * 32 + b;
                 bits &= bits - 1;
             }
+            pos += __shfl_sync(0xffffffffu, incl, 31);
         }
     } else {
         int32_t* keys = reinterpret_cast<int32_t*>(sm);
