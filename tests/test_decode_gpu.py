@@ -51,7 +51,8 @@ def _check(api, w, what="", status_ok=True, **kw):
 # ------------------------------------------------------------------------------------
 
 @pytest.mark.parametrize("rows,width,maxlen", [(1, 1, 1), (7, 64, 300), (40, 2048, 5000), (9, 513, 70000),
-                                               (5, 2048, 262144), (3, 4096, 300000), (4, 8192, 2_000_000)])
+                                               (6, 8192, 8500), (5, 2048, 262144), (3, 4096, 300000),
+                                               (4, 8192, 2_000_000)])
 def test_resolve_bit_exact(api, rows, width, maxlen):
     g = np.random.default_rng(rows * 1000 + width)
     sel = g.integers(-3, maxlen + 50, size=(rows, width)).astype(np.int32)
@@ -149,6 +150,15 @@ def test_default_grid_prefers_unit_alignment(api, seqs, k, heads, width):
     if sms == 152 and (seqs, k, heads) in ((128, 1, 128), (64, 1, 64), (32, 4, 64), (8, 1, 64)):
         assert got == 128                    # the four large workloads' shapes on GB300
     assert api.decode_grid(seqs, k, heads, width, 5) == 5
+
+
+def test_default_grid_sizes_the_default_workspace(api):
+    """The workspace sized for the default grid equals the one sized for the grid that
+    dsa_mla_decode_grid reports."""
+    for seqs, k, heads, width in [(128, 1, 128, 2048), (64, 1, 64, 2048), (3, 1, 64, 300), (80, 1, 64, 2048)]:
+        c = api.decode_grid(seqs, k, heads, width)
+        assert c > 0
+        assert api.workspace_bytes(seqs, k, heads, width) == api.workspace_bytes(seqs, k, heads, width, c)
 
 
 def test_default_grid_decodes_whole_units_without_combine(api):
