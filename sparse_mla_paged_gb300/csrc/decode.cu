@@ -605,6 +605,7 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
     Tiles tl_next = segment_tokens(p, seg0);
     bool q_loaded = false;  // the current unit's query operand was loaded during the previous unit
     float c_next = p.qscale[static_cast<int64_t>(seg0.unit) * kHeadsPerCta + hq];
+    bool pv_seen = false;   // the P.V two tiles back was already waited for (rescale or epilogue)
     for (int i = 0; i < nseg; ++i) {
         const Segment s = s_next;
         const Tiles tl = tl_next;
@@ -740,7 +741,8 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
             l_part += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
             if (st == 0 && (tau == 2 || tau == 3)) DSA_TRACE_AT(p, 74 + 8 * (tau - 2));
             // P buffer tau%2 is free once the P.V two tiles back has finished reading it.
-            if (tau >= 2) warp_wait(p, barp(BAR_PVDONE0 + (tau & 1)), ((tau >> 1) - 1) & 1, abort_flag);
+            if (tau >= 2 && !pv_seen) warp_wait(p, barp(BAR_PVDONE0 + (tau & 1)), ((tau >> 1) - 1) & 1, abort_flag);
+            pv_seen = false;
             if (st == 0 && (tau == 2 || tau == 3)) DSA_TRACE_AT(p, 75 + 8 * (tau - 2));
             const uint32_t pb = sbase + kOffP + (tau & 1) * 2 * kPTermBytes;
 #pragma unroll
@@ -755,6 +757,7 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
                 // write lets that P.V run while this tile's probabilities are formed; this
                 // tile's P.V waits for the rescale through the P-full barrier below.
                 warp_wait(p, barp(BAR_PVDONE0 + ((tau - 1) & 1)), ((tau - 1) >> 1) & 1, abort_flag);
+                pv_seen = true;  // the next tile's P buffer is free
                 tc_fence_after();
                 // Both dim chunks of a 32-head block are loaded together (one load latency
                 // per block instead of one per chunk) and share the block's 32 factors.
@@ -793,6 +796,7 @@ __device__ void run_softmax(const DecodeParams& p, uint8_t* smem, uint32_t sbase
 
         // ---- epilogue ----
         warp_wait(p, barp(BAR_PVDONE0 + ((tau - 1) & 1)), ((tau - 1) >> 1) & 1, abort_flag);
+        pv_seen = true;
         if (st == 0 && i == 0) DSA_TRACE_AT(p, 17);
         tc_fence_after();
         const float lpair = l_part + __shfl_xor_sync(0xffffffffu, l_part, 1);
