@@ -41,7 +41,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # ncu (dram__bytes_read.sum + dram__bytes_write.sum) on the decode kernel as it is now. A
 # workload absent here reports traffic null; an entry is dropped whenever the decode
 # kernel changes, until it is counted again.
-MEASURED_TRAFFIC = {}
+MEASURED_TRAFFIC = {"pooled_128k": 153921536, "ragged": 72731648, "verify_k4": 67966976, "decode_batch": 8965888}
 
 
 # ----------------------------------------------------------------------------------------
