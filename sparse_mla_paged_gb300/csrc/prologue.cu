@@ -107,28 +107,42 @@ __device__ void resolve_row(const PrologueParams& p, int32_t r, uint32_t* sm, in
         const int32_t wbeg = warp * wpw;
         const int32_t wend = min(wbeg + wpw, nwords);
         int32_t mine = 0;
+#pragma unroll 4
         for (int32_t w = wbeg + lane; w < wend; w += 32) mine += __popc(sm[w]);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
         int32_t pos = block_exclusive_scan(lane == 0 ? mine : 0, scratch, &total);
         pos = __shfl_sync(0xffffffffu, pos, 0);
-        for (int32_t w0 = wbeg; w0 < wend; w0 += 32) {
-            const int32_t w = w0 + lane;
-            uint32_t bits = w < wend ? sm[w] : 0u;
-            const int32_t c = __popc(bits);
-            int32_t incl = c;
+        // Four steps of 32 words at a time: their warp scans are independent and interleave.
+        constexpr int kSteps = 4;
+        for (int32_t w0 = wbeg; w0 < wend; w0 += 32 * kSteps) {
+            uint32_t bits[kSteps];
+            int32_t c[kSteps], incl[kSteps];
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
+            for (int j = 0; j < kSteps; ++j) {
+                const int32_t w = w0 + 32 * j + lane;
+                bits[j] = w < wend ? sm[w] : 0u;
+                c[j] = __popc(bits[j]);
+                incl[j] = c[j];
             }
-            int32_t at = pos + incl - c;
-            while (bits) {
-                const int b = __ffs(bits) - 1;
-                ids_s[at++] = w * 32 + b;
-                bits &= bits - 1;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1)
+#pragma unroll
+                for (int j = 0; j < kSteps; ++j) {
+                    const int32_t y = __shfl_up_sync(0xffffffffu, incl[j], o);
+                    if (lane >= o) incl[j] += y;
+                }
+#pragma unroll
+            for (int j = 0; j < kSteps; ++j) {
+                int32_t at = pos + incl[j] - c[j];
+                const int32_t w = w0 + 32 * j + lane;
+                while (bits[j]) {
+                    const int b = __ffs(bits[j]) - 1;
+                    ids_s[at++] = w * 32 + b;
+                    bits[j] &= bits[j] - 1;
+                }
+                pos += __shfl_sync(0xffffffffu, incl[j], 31);
             }
-            pos += __shfl_sync(0xffffffffu, incl, 31);
         }
     } else {
         int32_t* keys = reinterpret_cast<int32_t*>(sm);
