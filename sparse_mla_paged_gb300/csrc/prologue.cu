@@ -71,17 +71,20 @@ __device__ void resolve_row(const PrologueParams& p, int32_t r, uint32_t* sm, in
     long long* offs = p.block_tables ? p.offs + static_cast<int64_t>(r) * W : nullptr;
     int32_t total = 0;
     // The first batch of the selection row is requested together with the row's length
-    // (before the branch on it), and arrives while the bitmap is cleared.
+    // (before the branch on it), and arrives while the whole bitmap is cleared: clearing
+    // all of it does not wait for the length (the sort path overwrites it anyway).
     int32_t idv[kBatch];
 #pragma unroll
     for (int k = 0; k < kBatch; ++k) {
         const int32_t j = tid + k * kResolveThreads;
         idv[k] = j < W ? sel[j] : -1;
     }
+    uint4* sm4 = reinterpret_cast<uint4*>(sm);
+#pragma unroll
+    for (int k = 0; k < kBitmapWords / 4 / kResolveThreads; ++k)
+        sm4[tid + k * kResolveThreads] = make_uint4(0u, 0u, 0u, 0u);
     if (L <= kBitmapWords * 32) {
         const int32_t nwords = (L + 31) >> 5;
-        uint4* sm4 = reinterpret_cast<uint4*>(sm);
-        for (int32_t w = tid; w < (nwords + 3) >> 2; w += kResolveThreads) sm4[w] = make_uint4(0u, 0u, 0u, 0u);
         __syncthreads();
         for (int32_t j0 = tid;; j0 += kBatch * kResolveThreads) {
 #pragma unroll
@@ -145,6 +148,7 @@ __device__ void resolve_row(const PrologueParams& p, int32_t r, uint32_t* sm, in
             }
         }
     } else {
+        __syncthreads();  // the clearing above is done before the keys overwrite it
         int32_t* keys = reinterpret_cast<int32_t*>(sm);
         int32_t n = 1;
         while (n < W) n <<= 1;
