@@ -60,7 +60,8 @@ __device__ __forceinline__ float piece_weight(float lse, float m, float f) {
 // kFast > 0 (the host's bound on pieces per unit): the pieces' partial slots are found
 // before the grid-dependency wait (they depend on the partition only), then every thread
 // loads its 16-byte slice of every piece at once while the weight lanes load the lse
-// values: one round trip. kFast = 0: any number of pieces, kWeightChunk at a time.
+// values: one round trip. kFast = 0: any number of pieces, kWeightChunk at a time, one
+// round trip per chunk with a running maximum.
 template <int kFast, bool kNarrow>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams p) {
     // After a long decode the next call's first kernel may launch now (it waits for this
@@ -68,6 +69,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
     if (p.early_dependents) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __shared__ int32_t slot_s[kCombineThreads];
     __shared__ float w_s[kCombineWarps][kWeightChunk][8];
+    __shared__ __align__(16) float a_s[kCombineWarps][8];  // per-head factors of the generic path
     __shared__ __align__(16) __nv_bfloat16 out_s[kHeadsPerCta][kCombineDims];  // the block's output tile
     const int64_t u = blockIdx.x;
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
@@ -137,7 +139,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
 #pragma unroll
         for (int k = 0; k < kN; ++k)
             if (k < n) fold(raw[k], k);
-    } else {
+    } else if constexpr (kFast > 0) {
+        // More pieces than the variant's bound (the host never launches it so): the plain
+        // loop, piece by piece.
         asm volatile("griddepcontrol.wait;" ::: "memory");
         // Maximum and sum over every piece, per head (lanes 0..7 of each warp).
         float m = kNegInfC, sum = 0.0f;
@@ -165,6 +169,62 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
             for (int k = 0; k < n; ++k)
                 if (slot_s[k] >= 0) fold(slice(slot_s[k]), k);
         }
+    } else {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        // Any number of pieces, kWeightChunk at a time, in one pass: each chunk's slices and
+        // log-sum-exps are all requested at once (one round trip per chunk), and the fold
+        // keeps a running maximum per head (lanes 0..7 of each warp), rescaling what it has
+        // accumulated when the maximum rises; the sum of the weights divides at the end.
+        float m_run = kNegInfC, s_run = 0.0f;
+        for (int64_t k0 = 0; k0 < npieces; k0 += kWeightChunk) {
+            const int n = static_cast<int>(min(npieces - k0, static_cast<int64_t>(kWeightChunk)));
+            __syncthreads();  // the previous chunk's slots and weights are no longer read
+            if (t < n) slot_s[t] = piece_slot<kNarrow>(p.part, u, c_lo + k0 + t);
+            __syncthreads();
+            uint4 raw[kWeightChunk];
+#pragma unroll
+            for (int k = 0; k < kWeightChunk; ++k) {
+                raw[k] = make_uint4(0, 0, 0, 0);
+                if (k < n && slot_s[k] >= 0) raw[k] = slice(slot_s[k]);
+            }
+            if (lane < 8) {
+                float lse[kWeightChunk];
+                float cm = kNegInfC;
+#pragma unroll
+                for (int k = 0; k < kWeightChunk; ++k) {
+                    lse[k] = (k < n && slot_s[k] >= 0) ? lse_of(slot_s[k]) : kNegInfC;
+                    cm = fmaxf(cm, lse[k]);
+                }
+                const float m_new = fmaxf(m_run, cm);
+                const float a = m_run != kNegInfC ? exp2f(m_run - m_new) : 0.0f;
+                s_run *= a;
+#pragma unroll
+                for (int k = 0; k < kWeightChunk; ++k) {
+                    const float w = piece_weight(lse[k], m_new, 1.0f);
+                    s_run += w;
+                    w_s[warp][k][lane] = w;
+                }
+                a_s[warp][lane] = a;
+                m_run = m_new;
+            }
+            __syncwarp();
+            const float4 aa = *reinterpret_cast<const float4*>(&a_s[warp][0]);
+            const float4 ab = *reinterpret_cast<const float4*>(&a_s[warp][4]);
+            const float av[8] = {aa.x, aa.y, aa.z, aa.w, ab.x, ab.y, ab.z, ab.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] *= av[e];
+#pragma unroll
+            for (int k = 0; k < kWeightChunk; ++k)
+                if (k < n) fold(raw[k], k);
+        }
+        __syncwarp();
+        if (lane < 8) a_s[warp][lane] = s_run > 0.0f ? p.v_scale / s_run : 0.0f;
+        __syncwarp();
+        const float4 fa = *reinterpret_cast<const float4*>(&a_s[warp][0]);
+        const float4 fb = *reinterpret_cast<const float4*>(&a_s[warp][4]);
+        const float fv[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] *= fv[e];
     }
     // The block's output tile [64 heads][32 dims] goes through shared memory, so that each
     // thread writes 16 bytes (8 dims of one head) of the BF16 output rows.
