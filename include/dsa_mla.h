@@ -151,8 +151,9 @@ int32_t dsa_mla_decode_grid(int32_t num_seqs, int32_t rows_per_seq, int32_t num_
  *  num_ctas       decode grid size; 0 = default (dsa_mla_decode_grid: at most the SM count).
  *                 Must match the num_ctas the workspace was sized for.
  *  tile_tokens    KV tokens per decode tile: 0 = automatic (64-token tiles when each
- *                 decode CTA has at most 256 selected slots of work, 128 otherwise),
- *                 64 or 128 = that size. Any other value is DSA_ERR_INVALID_ARGUMENT.
+ *                 decode CTA has at most 256 selected slots of work or when k_cache and
+ *                 v_cache are different buffers, 128 otherwise), 64 or 128 = that size.
+ *                 Any other value is DSA_ERR_INVALID_ARGUMENT.
  *  gather_mode    how the decode fetches cache rows: 0 = default (per-thread 16-byte
  *                 copies), 1 = per-thread copies, 2 = tensor-map four-row gathers when
  *                 the pages are dense (cache_stride_bytes = block_size*512) and the caches

@@ -284,7 +284,11 @@ int32_t enqueue(const Args& a, const Plan& pl, uint8_t* ws, const CallOptions& o
         if (cs == cudaStreamCaptureStatusActive) ev_flags = cudaEventRecordExternal;
     }
     if (ev0 && cudaEventRecordWithFlags(ev0, stream, ev_flags) != cudaSuccess) return DSA_ERR_CUDA;
-    st = from_cuda(pl.small_tiles ? launch_decode_64(dp, kmap, vmap, stream) : launch_decode_128(dp, kmap, vmap, stream));
+    // With K and V in separate buffers a ring slot holds both tiles, so 128-token tiles would
+    // leave a single slot and no pipelining: such calls take 64-token tiles (three slots)
+    // unless the caller fixed the tile size (measured on ragged: 85 against 46 us per call).
+    const bool small = pl.small_tiles || (opt.tile_tokens == 0 && !dp.kv_same);
+    st = from_cuda(small ? launch_decode_64(dp, kmap, vmap, stream) : launch_decode_128(dp, kmap, vmap, stream));
     if (st != DSA_OK) return st;
     if (ev1 && cudaEventRecordWithFlags(ev1, stream, ev_flags) != cudaSuccess) return DSA_ERR_CUDA;
 
