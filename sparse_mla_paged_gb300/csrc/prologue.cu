@@ -6,8 +6,9 @@
 // and (for the decode) each id's cache byte offset through the block table
 // (decode_k.rs: physical = block_table[pos / block_size], slot = physical*block_size +
 // pos % block_size), so the decode's gather needs one load per token.
-//   * L <= 262144: a bitmap of L bits in shared memory; ids set with atomicOr and
-//     written out by a block-wide prefix count, which yields them sorted.
+//   * L <= 16 * 262144: a bitmap of 262144 bits in shared memory per window of that many
+//     positions, windows in ascending order (one for L <= 262144); ids set with atomicOr
+//     and written out by a block-wide prefix count, which yields them sorted.
 //   * longer rows: bitonic sort of the row in shared memory, then a prefix count of
 //     first occurrences.
 // Blocks [rows, rows + rows*groups) turn one (row, 64-head group) of BF16 queries into
@@ -27,6 +28,7 @@ constexpr int kMaxSel = DSA_MAX_SEL_WIDTH;                        // resolved id
 constexpr int kPrologueSmem = kBitmapWords * 4 + kMaxSel * 4;     // bitmap or keys, then the ids
 static_assert(kQImageBytes <= kPrologueSmem, "a query block stages its image in the same shared memory");
 constexpr int kBatch = 8;                                         // loads in flight per thread
+constexpr int kMaxWindows = 16;  // bitmap windows per row (4M positions); longer rows are sorted
 
 __device__ __forceinline__ int32_t row_seq_len(const PrologueParams& p, int32_t r) {
     int32_t L = p.verify_rows ? p.seq_lens[r / p.rows_per_seq] + (r % p.rows_per_seq) + 1 : p.seq_lens[r];
@@ -83,69 +85,92 @@ __device__ void resolve_row(const PrologueParams& p, int32_t r, uint32_t* sm, in
 #pragma unroll
     for (int k = 0; k < kBitmapWords / 4 / kResolveThreads; ++k)
         sm4[tid + k * kResolveThreads] = make_uint4(0u, 0u, 0u, 0u);
-    if (L <= kBitmapWords * 32) {
-        const int32_t nwords = (L + 31) >> 5;
-        __syncthreads();
-        for (int32_t j0 = tid;; j0 += kBatch * kResolveThreads) {
+    // Rows up to kMaxWindows bitmaps long are resolved one window of kBitmapWords*32
+    // positions at a time, in ascending order (one window for L <= 262144): mark the ids
+    // that fall in the window, then count and extract them after the ids of the windows
+    // before. The first window's ids come from the batch already loaded; a later window
+    // reads the row again (from L2).
+    const int32_t nwin = static_cast<int32_t>((static_cast<int64_t>(L) + kBitmapWords * 32 - 1) / (kBitmapWords * 32));
+    if (nwin <= kMaxWindows) {
+        for (int32_t win = 0; win < nwin; ++win) {
+            const int32_t lo = win * (kBitmapWords * 32);
+            const int32_t hi = min(L, lo + kBitmapWords * 32);
+            const int32_t nwords = (hi - lo + 31) >> 5;
+            if (win > 0) {
+                __syncthreads();  // the previous window's extraction has read the bitmap
 #pragma unroll
-            for (int k = 0; k < kBatch; ++k) {
-                const int32_t id = idv[k];
-                if (id >= 0 && id < L) atomicOr(&sm[id >> 5], 1u << (id & 31));
-            }
-            const int32_t n0 = j0 + kBatch * kResolveThreads;
-            if (n0 - tid >= W) break;
+                for (int k = 0; k < kBitmapWords / 4 / kResolveThreads; ++k)
+                    sm4[tid + k * kResolveThreads] = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-            for (int k = 0; k < kBatch; ++k) {
-                const int32_t j = n0 + k * kResolveThreads;
-                idv[k] = j < W ? sel[j] : -1;
+                for (int k = 0; k < kBatch; ++k) {
+                    const int32_t j = tid + k * kResolveThreads;
+                    idv[k] = j < W ? sel[j] : -1;
+                }
             }
-        }
-        __syncthreads();
-        // Each warp takes a contiguous range of words (a multiple of 32) and reads it 32
-        // consecutive words at a time (one word per lane, free of bank conflicts): a count
-        // pass, a block scan of the warp totals, then an extraction pass in which a warp
-        // scan of the words' bit counts places every lane's ids.
-        const int lane = tid & 31, warp = tid >> 5;
-        const int32_t wpw = ((nwords + kResolveThreads - 1) / kResolveThreads) * 32;
-        const int32_t wbeg = warp * wpw;
-        const int32_t wend = min(wbeg + wpw, nwords);
-        int32_t mine = 0;
+            __syncthreads();
+            for (int32_t j0 = tid;; j0 += kBatch * kResolveThreads) {
+#pragma unroll
+                for (int k = 0; k < kBatch; ++k) {
+                    const int32_t id = idv[k];
+                    if (id >= lo && id < hi) atomicOr(&sm[(id - lo) >> 5], 1u << ((id - lo) & 31));
+                }
+                const int32_t n0 = j0 + kBatch * kResolveThreads;
+                if (n0 - tid >= W) break;
+#pragma unroll
+                for (int k = 0; k < kBatch; ++k) {
+                    const int32_t j = n0 + k * kResolveThreads;
+                    idv[k] = j < W ? sel[j] : -1;
+                }
+            }
+            __syncthreads();
+            // Each warp takes a contiguous range of words (a multiple of 32) and reads it 32
+            // consecutive words at a time (one word per lane, free of bank conflicts): a count
+            // pass, a block scan of the warp totals, then an extraction pass in which a warp
+            // scan of the words' bit counts places every lane's ids.
+            const int lane = tid & 31, warp = tid >> 5;
+            const int32_t wpw = ((nwords + kResolveThreads - 1) / kResolveThreads) * 32;
+            const int32_t wbeg = warp * wpw;
+            const int32_t wend = min(wbeg + wpw, nwords);
+            int32_t mine = 0;
 #pragma unroll 4
-        for (int32_t w = wbeg + lane; w < wend; w += 32) mine += __popc(sm[w]);
+            for (int32_t w = wbeg + lane; w < wend; w += 32) mine += __popc(sm[w]);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
-        int32_t pos = block_exclusive_scan(lane == 0 ? mine : 0, scratch, &total);
-        pos = __shfl_sync(0xffffffffu, pos, 0);
-        // Four steps of 32 words at a time: their warp scans are independent and interleave.
-        constexpr int kSteps = 4;
-        for (int32_t w0 = wbeg; w0 < wend; w0 += 32 * kSteps) {
-            uint32_t bits[kSteps];
-            int32_t c[kSteps], incl[kSteps];
-#pragma unroll
-            for (int j = 0; j < kSteps; ++j) {
-                const int32_t w = w0 + 32 * j + lane;
-                bits[j] = w < wend ? sm[w] : 0u;
-                c[j] = __popc(bits[j]);
-                incl[j] = c[j];
-            }
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1)
+            for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+            int32_t wtotal = 0;
+            int32_t pos = block_exclusive_scan(lane == 0 ? mine : 0, scratch, &wtotal);
+            pos = __shfl_sync(0xffffffffu, pos, 0) + total;
+            // Four steps of 32 words at a time: their warp scans are independent and interleave.
+            constexpr int kSteps = 4;
+            for (int32_t w0 = wbeg; w0 < wend; w0 += 32 * kSteps) {
+                uint32_t bits[kSteps];
+                int32_t c[kSteps], incl[kSteps];
 #pragma unroll
                 for (int j = 0; j < kSteps; ++j) {
-                    const int32_t y = __shfl_up_sync(0xffffffffu, incl[j], o);
-                    if (lane >= o) incl[j] += y;
+                    const int32_t w = w0 + 32 * j + lane;
+                    bits[j] = w < wend ? sm[w] : 0u;
+                    c[j] = __popc(bits[j]);
+                    incl[j] = c[j];
                 }
 #pragma unroll
-            for (int j = 0; j < kSteps; ++j) {
-                int32_t at = pos + incl[j] - c[j];
-                const int32_t w = w0 + 32 * j + lane;
-                while (bits[j]) {
-                    const int b = __ffs(bits[j]) - 1;
-                    ids_s[at++] = w * 32 + b;
-                    bits[j] &= bits[j] - 1;
+                for (int o = 1; o < 32; o <<= 1)
+#pragma unroll
+                    for (int j = 0; j < kSteps; ++j) {
+                        const int32_t y = __shfl_up_sync(0xffffffffu, incl[j], o);
+                        if (lane >= o) incl[j] += y;
+                    }
+#pragma unroll
+                for (int j = 0; j < kSteps; ++j) {
+                    int32_t at = pos + incl[j] - c[j];
+                    const int32_t w = w0 + 32 * j + lane;
+                    while (bits[j]) {
+                        const int b = __ffs(bits[j]) - 1;
+                        ids_s[at++] = lo + w * 32 + b;
+                        bits[j] &= bits[j] - 1;
+                    }
+                    pos += __shfl_sync(0xffffffffu, incl[j], 31);
                 }
-                pos += __shfl_sync(0xffffffffu, incl[j], 31);
             }
+            total += wtotal;
         }
     } else {
         __syncthreads();  // the clearing above is done before the keys overwrite it

@@ -52,7 +52,7 @@ def _check(api, w, what="", status_ok=True, **kw):
 
 @pytest.mark.parametrize("rows,width,maxlen", [(1, 1, 1), (7, 64, 300), (40, 2048, 5000), (9, 513, 70000),
                                                (6, 8192, 8500), (5, 2048, 262144), (3, 4096, 300000),
-                                               (4, 8192, 2_000_000)])
+                                               (4, 8192, 2_000_000), (3, 2048, 5_000_000)])
 def test_resolve_bit_exact(api, rows, width, maxlen):
     g = np.random.default_rng(rows * 1000 + width)
     sel = g.integers(-3, maxlen + 50, size=(rows, width)).astype(np.int32)
